@@ -1,0 +1,386 @@
+"""Benchmark of the quantised-KV decode step on GB300.
+
+One step = for each of R independent layer caches (R chosen so their bytes
+exceed L2 several times): append one token's K/V (q8_0 / q5_1 quantise +
+commit), decode attention of one query row over the whole cache (split +
+merge kernels), and truncate the appended row again (rollback to
+snapshot_len + 0), so every step sees the same length.  Inputs are resident in
+HBM before the timed region; decode launches are bracketed by CUDA events on
+the launching stream to time the dominant kernel pair.
+
+`value` is GB/s of quantised KV read by the decode (algorithmic bytes: every
+visible row x (K 34 + V 24 bytes per 32 elements)), summed over all ranks.
+`e2e` repeats the step through the same public API with the step's inputs
+copied from pinned host memory and the attention output copied back inside
+the timed region.  `--impl reference` times the fp64 CPU oracle on a bounded
+sample of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       [--layers R] [--impl kvq|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_kv_cache_08_gb300 import build as kbuild  # noqa: E402
+from quantized_kv_cache_08_gb300.inputs import workload  # noqa: E402
+
+METRIC = "decode-attn GB/s of quantized KV read (fraction of HBM peak); tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def kv_bytes_per_row(wl):
+    kb = wl.n_kv * wl.head_dim // 32
+    return kb * (34 + 24)
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(os.path.join(ROOT, "quantized_kv_cache_08_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "quantized_kv_cache_08_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(name):
+    """dram bytes per decode launch from a committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(name)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_decode")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kvq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x, world):
+    """Largest value of x over ranks (the job's time); x on every rank."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_kvq(args, world, rank, local):
+    from quantized_kv_cache_08_gb300.cache import KVCache
+
+    kbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workload(args.workload)
+    if wl.name not in ("ctx32k", "ctx512", "batch64"):
+        raise SystemExit("bench.py times the flat T=1 decode workloads (ctx32k, ctx512, batch64)")
+    lens = wl.lengths()
+    row_bytes = kv_bytes_per_row(wl)
+    footprint = sum(lens) * row_bytes
+    R = args.layers or max(1, math.ceil(3 * L2_BYTES / footprint))
+    T = 1
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+
+    # --- build R layer caches holding len-1 rows each (prefill, untimed)
+    caches = []
+    for r in range(R):
+        c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=64, max_rows=max(lens))
+        for b, L in enumerate(lens):
+            k, v = wl.kv(b + 1000 * r + 100000 * rank, 0, L - 1)
+            kd, vd = k.to(dev), v.to(dev)
+            for t0 in range(0, L - 1, 64):
+                t1 = min(L - 1, t0 + 64)
+                c.append(kd[t0:t1].unsqueeze(0), vd[t0:t1].unsqueeze(0), seq_ids=[b])
+        caches.append(c)
+    base_len = [L - 1 for L in lens]
+    # --- per-layer step inputs, resident on the device
+    k_new, v_new, qs = [], [], []
+    for r in range(R):
+        kk = torch.stack([wl.kv(b + 1000 * r + 100000 * rank, L - 1, L)[0] for b, L in enumerate(lens)])
+        vv = torch.stack([wl.kv(b + 1000 * r + 100000 * rank, L - 1, L)[1] for b, L in enumerate(lens)])
+        k_new.append(kk.to(dev))
+        v_new.append(vv.to(dev))
+        qs.append(wl.q(r + 7 * rank, T=T).to(dev))
+    outs = [torch.empty(wl.n_seq, T, wl.n_q, wl.head_dim, dtype=torch.float32, device=dev)
+            for _ in range(R)]
+    torch.cuda.synchronize()
+
+    def step(events=None):
+        for r, c in enumerate(caches):
+            c.append(k_new[r], v_new[r])
+            if events is not None:
+                events[r][0].record(stream)
+            c.decode(qs[r], out=outs[r])
+            if events is not None:
+                events[r][1].record(stream)
+            c.truncate(base_len)
+
+    # eager warm-up (kernel attributes, lazy module loads), then capture: one
+    # step for the untimed warm-up replays, K steps with event nodes around
+    # every decode for the timed replay.  The counters live on the device, so
+    # the captured append / decode / truncate replay with the right lengths.
+    step()
+    torch.cuda.synchronize()
+    g_warm = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_warm, stream=stream):
+        step()
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
+          for _ in range(args.steps)]
+    g_timed = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_timed, stream=stream):
+        for k in range(args.steps):
+            step(ev[k])
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        g_warm.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    g_timed.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    dec_ms = sum(a.elapsed_time(b) for evk in ev for a, b in evk)
+    dec_ms = max_over_ranks(dec_ms, world)
+    for c in caches:
+        if c.device_error() != 0:
+            raise SystemExit("device error word set during the benchmark")
+
+    kv_bytes_step = R * sum(lens) * row_bytes           # per rank
+    decodes = args.steps * R
+    value = world * kv_bytes_step * args.steps / (dec_ms * 1e-3) / 1e9
+    tokens_per_s = world * wl.n_seq * T * decodes / (dec_ms * 1e-3)
+    achieved = kv_bytes_step * args.steps / (dec_ms * 1e-3) / 1e9  # per GPU
+    peak, peak_src = measured_peak()
+
+    # --- end to end through the public API: pinned host inputs in, output out
+    pin_k = [x.cpu().pin_memory() for x in k_new]
+    pin_v = [x.cpu().pin_memory() for x in v_new]
+    pin_q = [x.cpu().pin_memory() for x in qs]
+    pin_o = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    dk = [torch.empty_like(x) for x in k_new]
+    dv = [torch.empty_like(x) for x in v_new]
+    dq = [torch.empty_like(x) for x in qs]
+
+    def e2e_step():
+        for r, c in enumerate(caches):
+            dk[r].copy_(pin_k[r], non_blocking=True)
+            dv[r].copy_(pin_v[r], non_blocking=True)
+            dq[r].copy_(pin_q[r], non_blocking=True)
+            c.append(dk[r], dv[r])
+            c.decode(dq[r], out=outs[r])
+            pin_o[r].copy_(outs[r], non_blocking=True)
+            c.truncate(base_len)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    h2d = sum(x.numel() * x.element_size() for x in pin_k + pin_v + pin_q)
+    d2h = sum(x.numel() * x.element_size() for x in pin_o)
+    e2e_value = world * kv_bytes_step * args.steps / (e2e_ms * 1e-3) / 1e9
+
+    cfg = {"workload": f"{wl.name}: {wl.n_seq} seq, {wl.n_q} Q / {wl.n_kv} KV heads, head_dim "
+                       f"{wl.head_dim}, {sum(lens)} rows, T=1, q {wl.q_dtype}, K q8_0 / V q5_1",
+           "layers": R, "rows_total": sum(lens),
+           "kv_bytes_per_decode": sum(lens) * row_bytes,
+           "step": "per layer: append 1 row + decode + truncate back",
+           "l2": f"inputs larger than L2: {R} layer caches, {R * footprint / 1e6:.0f} MB rotated"}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": cfg,
+        "tokens_per_s": round(tokens_per_s, 1),
+        "decode_ms_per_layer": round(dec_ms / decodes, 5),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
+                     "kernel": "kvq decode (split + merge)"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4)},
+        "gpu_launches": 5 * R * args.steps,
+        "timing": "CUDA graph of K steps, event nodes around each decode",
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, lens)
+    return line
+
+
+def cpu_baseline(wl, lens, budget_s=12.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload: the
+    decode of one layer for the first sequence (quantise its rows once, then
+    dequantise + attend per repetition)."""
+    from oracle import kvq_oracle as O
+
+    L = lens[0]
+    k, v = wl.kv(0, 0, L)
+    ora = O.OracleKvCache(1, wl.n_kv, wl.head_dim)
+    ora.append(k.unsqueeze(0).numpy(), v.unsqueeze(0).numpy())
+    q = wl.q(0, T=1)[:1].float().numpy().astype("float64")
+    reps, t_total = 0, 0.0
+    while t_total < budget_s and reps < 20:
+        t = time.perf_counter()
+        ora.decode(q)
+        t_total += time.perf_counter() - t
+        reps += 1
+    gbs = reps * L * kv_bytes_per_row(wl) / t_total / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{reps} fp64 decodes of 1 sequence x {L} rows ({wl.name}), "
+                      f"numpy with its default BLAS threading, {t_total:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: K timed steps, each a bounded sample."""
+    if rank != 0:
+        return None
+    wl = workload(args.workload)
+    lens = wl.lengths()
+    base = cpu_baseline(wl, lens, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    return {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "sample": base["sample"]},
+            "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="ctx32k")
+    ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_kvq(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,129 @@
+"""A torch-facing holder for one kvq layer cache.
+
+PyTorch only provides the device memory (uint8 / int32 tensors) and the
+stream; every operation is one call through the C ABI (see _binding).
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import _binding as B
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return B.KVQ_F32
+    if t.dtype == torch.bfloat16:
+        return B.KVQ_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+
+
+def _check_dev(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class KVCache:
+    """n_seq sequences of one attention layer: q8_0 K plane, q5_1 V plane,
+    device counters and the decode workspace, all caller-owned torch memory."""
+
+    def __init__(self, n_seq, n_kv_heads, head_dim, max_q_heads, max_t=1, max_rows=0,
+                 window=0, ring=False, device=None, stream=None):
+        self.cfg = B.make_config(n_seq, n_kv_heads, head_dim, max_q_heads, max_t, max_rows,
+                                 window, ring)
+        sz = B.kvq_required_bytes(self.cfg)
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        self.k_plane = torch.empty(sz.k_plane, dtype=torch.uint8, device=dev)
+        self.v_plane = torch.empty(sz.v_plane, dtype=torch.uint8, device=dev)
+        self.counters = torch.empty(sz.counters // 4, dtype=torch.int32, device=dev)
+        self.workspace = torch.empty(max(sz.workspace, 16), dtype=torch.uint8, device=dev)
+        self.n_seq, self.n_kv_heads, self.head_dim = n_seq, n_kv_heads, head_dim
+        kb = n_kv_heads * head_dim // 32
+        self.k_tok, self.v_tok = kb * 34, kb * 24
+        self.rows = sz.k_plane // (n_seq * self.k_tok)
+        self.window, self.ring = window, bool(ring)
+        self.handle = B.kvq_alloc(self.cfg, self.k_plane.data_ptr(), self.v_plane.data_ptr(),
+                                  self.counters.data_ptr(), self.workspace.data_ptr(),
+                                  _stream_handle(stream))
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None:
+            B.kvq_free(h)
+            self.handle = None
+
+    # -- the four calls of the path
+    def append(self, k, v, seq_ids=None, stream=None):
+        """k, v: [n, T, Hkv, D] float32/bfloat16 CUDA tensors."""
+        _check_dev(k, "k")
+        _check_dev(v, "v")
+        if k.shape != v.shape or k.dtype != v.dtype or k.dim() != 4:
+            raise ValueError("k and v must both be [n, T, Hkv, D] of one dtype")
+        n = self.n_seq if seq_ids is None else len(seq_ids)
+        if k.shape[0] != n or k.shape[2] != self.n_kv_heads or k.shape[3] != self.head_dim:
+            raise ValueError(f"k shape {tuple(k.shape)} does not match the cache")
+        B.kvq_append(self.handle, k.data_ptr(), v.data_ptr(), _dtype_code(k), k.shape[1],
+                     seq_ids, _stream_handle(stream))
+
+    def decode(self, q, sinks=None, scale=0.0, out=None, stream=None):
+        """q: [n_seq, T, Hq, D] float32/bfloat16; returns float32 [n_seq, T, Hq, D]."""
+        _check_dev(q, "q")
+        if q.dim() != 4 or q.shape[0] != self.n_seq or q.shape[3] != self.head_dim:
+            raise ValueError(f"q shape {tuple(q.shape)} does not match the cache")
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        _check_dev(out, "out")
+        if out.dtype != torch.float32 or out.shape != q.shape:
+            raise ValueError("out must be float32 with q's shape")
+        sp = None
+        if sinks is not None:
+            _check_dev(sinks, "sinks")
+            if sinks.dtype != torch.float32 or sinks.numel() != q.shape[2]:
+                raise ValueError("sinks must be float32 [Hq]")
+            sp = sinks.data_ptr()
+        B.kvq_decode(self.handle, q.data_ptr(), _dtype_code(q), q.shape[1], q.shape[2], sp,
+                     scale, out.data_ptr(), _stream_handle(stream))
+        return out
+
+    def truncate(self, new_len, stream=None):
+        B.kvq_truncate(self.handle, list(new_len), _stream_handle(stream))
+
+    # -- host-side helpers
+    def lens(self):
+        return B.kvq_get_len(self.handle, self.n_seq)[0]
+
+    def bases(self):
+        return B.kvq_get_len(self.handle, self.n_seq)[1]
+
+    def note_replayed(self, steps, T):
+        B.kvq_note_replayed(self.handle, steps, T)
+
+    def ring_headroom(self, T):
+        return B.kvq_ring_headroom(self.handle, T)
+
+    def physical_rows(self, seq, start, end):
+        return B.kvq_physical_rows(self.handle, seq, start, end)
+
+    def device_error(self, stream=None):
+        return B.kvq_read_device_error(self.handle, _stream_handle(stream))
+
+    def set_split_rows(self, rows):
+        B.kvq_set_split_rows(self.handle, rows)
+
+    def k_rows(self, seq, phys_lo, phys_hi):
+        """Raw K bytes of physical rows [phys_lo, phys_hi) of a sequence (a view)."""
+        v = self.k_plane.view(self.n_seq, self.rows, self.k_tok)
+        return v[seq, phys_lo:phys_hi]
+
+    def v_rows(self, seq, phys_lo, phys_hi):
+        v = self.v_plane.view(self.n_seq, self.rows, self.v_tok)
+        return v[seq, phys_lo:phys_hi]

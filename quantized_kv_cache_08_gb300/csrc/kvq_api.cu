@@ -1,0 +1,467 @@
+// Host side of the kvq C ABI: validation against the host mirror of the
+// lengths, ring bookkeeping, workspace layout and kernel launches.  See
+// include/kvq.h for the contract of every entry point.
+#include "../../include/kvq.h"
+#include "kvq_internal.cuh"
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+using namespace kvq;
+
+struct kvq_cache {
+    kvq_config cfg;
+    uint8_t* k_plane;
+    uint8_t* v_plane;
+    int* len_d;
+    int* base_d;
+    int* err_d;
+    uint8_t* ws;
+    size_t off_part_o, off_part_ml, off_plan, off_scratch;
+    int kb, k_tok, v_tok, rows;          // rows = physical rows per sequence
+    int max_vis;                         // most rows one decode may read per sequence
+    int num_sms;
+    int split_rows;                      // 0 = automatic
+    std::vector<int> len, base;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+kvq_status fail(kvq_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+kvq_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(KVQ_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Geometry {
+    int kb, k_tok, v_tok, rows, max_vis;
+};
+
+kvq_status check_config(const kvq_config* c, Geometry* g) {
+    if (!c) return fail(KVQ_EINVAL, "config is NULL");
+    if (c->k_fmt != KVQ_Q8_0 || c->v_fmt != KVQ_Q5_1)
+        return fail(KVQ_EUNSUPPORTED, "formats must be K=q8_0, V=q5_1");
+    if (c->n_seq < 1 || c->n_seq > 4096) return fail(KVQ_EINVAL, "n_seq must be in [1, 4096]");
+    if (c->n_kv_heads < 1) return fail(KVQ_EINVAL, "n_kv_heads must be >= 1");
+    if (c->head_dim < 32 || c->head_dim > 512 || c->head_dim % 32)
+        return fail(KVQ_EINVAL, "head_dim must be a multiple of 32 in [32, 512] (a block never straddles a head)");
+    if (c->max_q_heads < c->n_kv_heads || c->max_q_heads % c->n_kv_heads)
+        return fail(KVQ_EINVAL, "max_q_heads must be a positive multiple of n_kv_heads");
+    if (c->max_t < 1 || c->max_t > 64) return fail(KVQ_EINVAL, "max_t must be in [1, 64]");
+    if (c->window < 0) return fail(KVQ_EINVAL, "window must be >= 0");
+    if (c->ring && c->window <= 0) return fail(KVQ_EINVAL, "a ring cache needs window > 0");
+    const long long kvd = (long long)c->n_kv_heads * c->head_dim;
+    if (kvd > 65536) return fail(KVQ_EINVAL, "n_kv_heads * head_dim too large");
+    g->kb = (int)(kvd / kQK);
+    g->k_tok = g->kb * kQ8Bytes;
+    g->v_tok = g->kb * kQ5Bytes;
+    if (c->ring) {
+        const int need = c->window + 30 + c->max_t;
+        g->rows = c->max_rows == 0 ? need : c->max_rows;
+        if (g->rows < need)
+            return fail(KVQ_EINVAL, "ring max_rows %d below window + 30 + max_t = %d", g->rows, need);
+        g->max_vis = std::min(g->rows, c->window + c->max_t - 1);
+    } else {
+        if (c->max_rows < 1) return fail(KVQ_EINVAL, "max_rows must be >= 1");
+        g->rows = c->max_rows;
+        g->max_vis = c->window > 0 ? std::min(g->rows, c->window + c->max_t - 1) : g->rows;
+    }
+    return KVQ_OK;
+}
+
+struct WsLayout {
+    size_t part_o, part_ml, plan, scratch, total;
+};
+
+WsLayout ws_layout(const kvq_config* c, const Geometry& g) {
+    WsLayout w;
+    const size_t items = (size_t)c->n_seq * ((g.max_vis + kMinSplitRows - 1) / kMinSplitRows);
+    const size_t recs = items * (size_t)c->max_q_heads * c->max_t;
+    w.part_o = 0;
+    w.part_ml = round_up(w.part_o + recs * c->head_dim * sizeof(float), 256);
+    w.plan = round_up(w.part_ml + recs * 2 * sizeof(float), 256);
+    w.scratch = round_up(w.plan + (c->n_seq + 1) * sizeof(int), 256);
+    w.total = w.scratch + (c->ring ? round_up((size_t)g.rows * (g.k_tok + g.v_tok), 256) : 0);
+    return w;
+}
+
+size_t counters_bytes(int n_seq) { return round_up((2 * (size_t)n_seq + 1) * sizeof(int), 256); }
+
+// visible-row start of a T-row step
+int vis_lo(const kvq_cache* c, int len, int T) {
+    return c->cfg.window > 0 ? std::max(0, len - T + 1 - c->cfg.window) : 0;
+}
+
+bool aligned16(const void* p) { return ((size_t)p & 15) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_last_error(void) { return g_err.c_str(); }
+
+int kvq_block_bytes(kvq_fmt fmt) {
+    if (fmt == KVQ_Q8_0) return kQ8Bytes;
+    if (fmt == KVQ_Q5_1) return kQ5Bytes;
+    return -1;
+}
+
+size_t kvq_bytes_per_token(const kvq_config* cfg) {
+    Geometry g;
+    if (check_config(cfg, &g) != KVQ_OK) return 0;
+    return (size_t)g.k_tok + g.v_tok;
+}
+
+kvq_status kvq_required_bytes(const kvq_config* cfg, kvq_sizes* out) {
+    Geometry g;
+    kvq_status st = check_config(cfg, &g);
+    if (st != KVQ_OK) return st;
+    if (!out) return fail(KVQ_EINVAL, "out is NULL");
+    out->k_plane = (size_t)cfg->n_seq * g.rows * g.k_tok;
+    out->v_plane = (size_t)cfg->n_seq * g.rows * g.v_tok;
+    out->counters = counters_bytes(cfg->n_seq);
+    out->workspace = ws_layout(cfg, g).total;
+    return KVQ_OK;
+}
+
+kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* counters, void* workspace,
+                     void* stream, kvq_cache** out) {
+    Geometry g;
+    kvq_status st = check_config(cfg, &g);
+    if (st != KVQ_OK) return st;
+    if (!out) return fail(KVQ_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (!k_plane || !v_plane || !counters || !workspace) return fail(KVQ_EINVAL, "a device buffer is NULL");
+    if (!aligned16(k_plane) || !aligned16(v_plane) || !aligned16(counters) || !aligned16(workspace))
+        return fail(KVQ_EINVAL, "device buffers must be 16-byte aligned");
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    kvq_cache* c = new kvq_cache();
+    c->cfg = *cfg;
+    c->cfg.max_rows = g.rows;
+    c->k_plane = static_cast<uint8_t*>(k_plane);
+    c->v_plane = static_cast<uint8_t*>(v_plane);
+    c->len_d = static_cast<int*>(counters);
+    c->base_d = c->len_d + cfg->n_seq;
+    c->err_d = c->base_d + cfg->n_seq;
+    c->ws = static_cast<uint8_t*>(workspace);
+    const WsLayout w = ws_layout(cfg, g);
+    c->off_part_o = w.part_o;
+    c->off_part_ml = w.part_ml;
+    c->off_plan = w.plan;
+    c->off_scratch = w.scratch;
+    c->kb = g.kb;
+    c->k_tok = g.k_tok;
+    c->v_tok = g.v_tok;
+    c->rows = g.rows;
+    c->max_vis = g.max_vis;
+    c->num_sms = sms;
+    c->split_rows = 0;
+    c->len.assign(cfg->n_seq, 0);
+    c->base.assign(cfg->n_seq, 0);
+    e = cudaMemsetAsync(counters, 0, counters_bytes(cfg->n_seq), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        delete c;
+        return cuda_fail(e, "cudaMemsetAsync(counters)");
+    }
+    *out = c;
+    return KVQ_OK;
+}
+
+void kvq_free(kvq_cache* cache) { delete cache; }
+
+kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, kvq_dtype dtype, int T, const int* seq_ids,
+                      int n_ids, void* stream) {
+    if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+    if (!k || !v) return fail(KVQ_EINVAL, "k or v is NULL");
+    if (dtype != KVQ_F32 && dtype != KVQ_BF16) return fail(KVQ_EINVAL, "dtype must be f32 or bf16");
+    if (T < 1 || T > c->cfg.max_t) return fail(KVQ_EINVAL, "T=%d outside [1, max_t=%d]", T, c->cfg.max_t);
+    const int B = c->cfg.n_seq;
+    std::vector<int> ids;
+    if (seq_ids) {
+        if (n_ids < 1 || n_ids > B) return fail(KVQ_EINVAL, "n_ids must be in [1, n_seq]");
+        ids.assign(seq_ids, seq_ids + n_ids);
+        std::vector<char> seen(B, 0);
+        for (int b : ids) {
+            if (b < 0 || b >= B) return fail(KVQ_EINVAL, "sequence index %d out of range", b);
+            if (seen[b]) return fail(KVQ_EINVAL, "sequence index %d repeated", b);
+            seen[b] = 1;
+        }
+    } else {
+        ids.resize(B);
+        for (int b = 0; b < B; ++b) ids[b] = b;
+    }
+    // capacity and ring decisions, all validated before anything is enqueued
+    const bool ring = c->cfg.ring != 0;
+    std::vector<int> new_base(ids.size());
+    for (size_t i = 0; i < ids.size(); ++i) {
+        const int b = ids[i];
+        const long long len = c->len[b];
+        int nb = c->base[b];
+        if (len + T - nb > c->rows) {
+            if (!ring)
+                return fail(KVQ_ERANGE, "sequence %d: len %lld + T %d exceeds max_rows %d", b, len, T, c->rows);
+            nb = (int)(std::max(0LL, len + 1 - c->cfg.window) & ~31LL);
+            if (len + T - nb > c->rows)
+                return fail(KVQ_ERANGE, "sequence %d: T %d does not fit the ring of %d rows", b, T, c->rows);
+        }
+        if (len + T > 0x7fffffffLL) return fail(KVQ_ERANGE, "sequence %d: length overflows int32", b);
+        new_base[i] = nb;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    // ring rebases: live rows [nb, len) move to physical row 0 through scratch
+    for (size_t i = 0; i < ids.size(); ++i) {
+        const int b = ids[i];
+        const int nb = new_base[i];
+        if (nb == c->base[b]) continue;
+        const int live = c->len[b] - nb;
+        const size_t src_row = (size_t)b * c->rows + (size_t)(nb - c->base[b]);
+        const size_t dst_row = (size_t)b * c->rows;
+        uint8_t* sk = c->ws + c->off_scratch;
+        uint8_t* sv = sk + (size_t)c->rows * c->k_tok;
+        const size_t kbytes = (size_t)live * c->k_tok, vbytes = (size_t)live * c->v_tok;
+        e = launch_ring_copy(c->k_plane + src_row * c->k_tok, c->v_plane + src_row * c->v_tok, sk, sv, kbytes,
+                             vbytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ring rebase copy");
+        e = launch_ring_copy(sk, sv, c->k_plane + dst_row * c->k_tok, c->v_plane + dst_row * c->v_tok, kbytes,
+                             vbytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ring rebase copy back");
+        e = launch_set_base(c->base_d, b, nb, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ring base update");
+        c->base[b] = nb;
+    }
+    AppendParams p;
+    p.k = k;
+    p.v = v;
+    p.bf16 = dtype == KVQ_BF16;
+    p.k_plane = c->k_plane;
+    p.v_plane = c->v_plane;
+    p.len_d = c->len_d;
+    p.base_d = c->base_d;
+    p.err_d = c->err_d;
+    p.T = T;
+    p.kb = c->kb;
+    p.k_tok = c->k_tok;
+    p.v_tok = c->v_tok;
+    p.max_rows = c->rows;
+    SeqIds sid;
+    for (size_t first = 0; first < ids.size(); first += kMaxIdsPerLaunch) {
+        const int n = (int)std::min(ids.size() - first, (size_t)kMaxIdsPerLaunch);
+        sid.n = n;
+        sid.identity = seq_ids ? 0 : 1;
+        sid.first = (int)first;
+        for (int i = 0; i < n; ++i) sid.id[i] = ids[first + i];
+        p.entry_offset = (long long)first;
+        e = launch_append(p, sid, s);
+        if (e != cudaSuccess) return cuda_fail(e, "append kernel");
+        e = launch_commit(c->len_d, sid, T, s);
+        if (e != cudaSuccess) return cuda_fail(e, "commit kernel");
+    }
+    for (int b : ids) c->len[b] += T;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n_q_heads, const float* sinks,
+                      float scale, float* out, void* stream) {
+    if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+    if (!q || !out) return fail(KVQ_EINVAL, "q or out is NULL");
+    if (dtype != KVQ_F32 && dtype != KVQ_BF16) return fail(KVQ_EINVAL, "dtype must be f32 or bf16");
+    if (T < 1 || T > c->cfg.max_t) return fail(KVQ_EINVAL, "T=%d outside [1, max_t=%d]", T, c->cfg.max_t);
+    const int Hkv = c->cfg.n_kv_heads;
+    if (n_q_heads < Hkv || n_q_heads % Hkv || n_q_heads > c->cfg.max_q_heads)
+        return fail(KVQ_EINVAL, "n_q_heads must be a multiple of n_kv_heads and <= max_q_heads");
+    if (c->k_tok % 16 || c->v_tok % 16)
+        return fail(KVQ_EUNSUPPORTED, "decode needs n_kv_heads*head_dim to be a multiple of 256");
+    const int B = c->cfg.n_seq;
+    const int D = c->cfg.head_dim;
+    const int hpk = n_q_heads / Hkv;
+    const int Q = hpk * T;
+    const int QC = Q <= 4 ? 4 : 8;
+    const int NBH = D / 32;
+    const int nK = (QC / 4) * Hkv * NBH;
+    if (2 * nK > kSplitThreads || kSplitThreads % (2 * nK))
+        return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
+    long long total_vis = 0;
+    for (int b = 0; b < B; ++b) {
+        if (c->len[b] < T) return fail(KVQ_ERANGE, "sequence %d holds %d rows, fewer than T=%d", b, c->len[b], T);
+        total_vis += c->len[b] - vis_lo(c, c->len[b], T);
+    }
+    // rows per split: one wave of items for one sequence, ~16 items per CTA otherwise
+    int C = c->split_rows;
+    if (C == 0) {
+        const long long per = B == 1 ? (total_vis + c->num_sms - 1) / c->num_sms
+                                     : (total_vis + 16LL * c->num_sms - 1) / (16LL * c->num_sms);
+        C = (int)std::max<long long>(kMinSplitRows, round_up((size_t)per, 8));
+    }
+    const int max_splits = (c->max_vis + C - 1) / C;
+
+    SplitParams p;
+    p.k_plane = c->k_plane;
+    p.v_plane = c->v_plane;
+    p.len_d = c->len_d;
+    p.base_d = c->base_d;
+    p.err_d = c->err_d;
+    p.q = q;
+    p.q_bf16 = dtype == KVQ_BF16;
+    p.qscale = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
+    p.B = B;
+    p.T = T;
+    p.Hq = n_q_heads;
+    p.Hkv = Hkv;
+    p.hpk = hpk;
+    p.D = D;
+    p.kb = c->kb;
+    p.k_tok = c->k_tok;
+    p.v_tok = c->v_tok;
+    p.max_rows = c->rows;
+    p.window = c->cfg.window;
+    p.C = C;
+    p.QC = QC;
+    p.nqs = (Q + QC - 1) / QC;
+    p.Qtot = n_q_heads * T;
+    p.part_o = reinterpret_cast<float*>(c->ws + c->off_part_o);
+    p.part_ml = reinterpret_cast<float*>(c->ws + c->off_part_ml);
+    p.plan = reinterpret_cast<int*>(c->ws + c->off_plan);
+    p.k_stage_bytes = (uint32_t)round_up((size_t)kTileRows * c->k_tok, 128);
+    p.stage_bytes = p.k_stage_bytes + (uint32_t)round_up((size_t)kTileRows * c->v_tok, 128);
+    const int smem_max = split_max_smem();
+    p.nstage = 4;
+    while (p.nstage > 2 && split_smem_bytes(p) > (size_t)smem_max) --p.nstage;
+    if (split_smem_bytes(p) > (size_t)smem_max)
+        return fail(KVQ_EUNSUPPORTED, "decode tile does not fit shared memory (%zu bytes)", split_smem_bytes(p));
+    long long items = 0;
+    for (int b = 0; b < B; ++b) {
+        const int vis = c->len[b] - vis_lo(c, c->len[b], T);
+        items += (vis + C - 1) / C;
+    }
+    items *= p.nqs;
+    const int grid = (int)std::max(1LL, std::min<long long>(items, c->num_sms));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_split(p, grid, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode split kernel");
+    MergeParams m;
+    m.part_o = p.part_o;
+    m.part_ml = p.part_ml;
+    m.plan = p.plan;
+    m.sinks = sinks;
+    m.out = out;
+    m.B = B;
+    m.Hq = n_q_heads;
+    m.Qtot = p.Qtot;
+    m.D = D;
+    e = launch_merge(m, T, max_splits, true, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode merge kernel");
+    return KVQ_OK;
+}
+
+kvq_status kvq_truncate(kvq_cache* c, const int* new_len, void* stream) {
+    if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+    if (!new_len) return fail(KVQ_EINVAL, "new_len is NULL");
+    const int B = c->cfg.n_seq;
+    for (int b = 0; b < B; ++b) {
+        const int n = new_len[b];
+        if (n < 0 || n > c->len[b])
+            return fail(KVQ_ERANGE, "sequence %d: new length %d outside [0, %d]", b, n, c->len[b]);
+        if (c->cfg.ring && std::max(0, n + 1 - c->cfg.window) < c->base[b])
+            return fail(KVQ_ERANGE, "sequence %d: rows below ring base %d are gone", b, c->base[b]);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    SeqIds sid;
+    for (int first = 0; first < B; first += kMaxIdsPerLaunch) {
+        const int n = std::min(B - first, kMaxIdsPerLaunch);
+        sid.n = n;
+        sid.identity = 1;
+        sid.first = first;
+        cudaError_t e = launch_set_len(c->len_d, sid, new_len + first, s);
+        if (e != cudaSuccess) return cuda_fail(e, "truncate kernel");
+    }
+    for (int b = 0; b < B; ++b) c->len[b] = new_len[b];
+    return KVQ_OK;
+}
+
+kvq_status kvq_get_len(const kvq_cache* c, int* len_host, int* base_host) {
+    if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+    for (int b = 0; b < c->cfg.n_seq; ++b) {
+        if (len_host) len_host[b] = c->len[b];
+        if (base_host) base_host[b] = c->base[b];
+    }
+    return KVQ_OK;
+}
+
+kvq_status kvq_note_replayed(kvq_cache* c, int steps, int T) {
+    if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+    if (steps < 0 || T < 1 || T > c->cfg.max_t) return fail(KVQ_EINVAL, "bad steps or T");
+    const long long add = (long long)steps * T;
+    for (int b = 0; b < c->cfg.n_seq; ++b)
+        if (c->len[b] + add - c->base[b] > c->rows)
+            return fail(KVQ_ERANGE, "sequence %d would exceed its physical rows", b);
+    for (int b = 0; b < c->cfg.n_seq; ++b) c->len[b] += (int)add;
+    return KVQ_OK;
+}
+
+kvq_status kvq_ring_headroom(const kvq_cache* c, int T, int* steps) {
+    if (!c || !steps) return fail(KVQ_EINVAL, "NULL argument");
+    if (T < 1 || T > c->cfg.max_t) return fail(KVQ_EINVAL, "bad T");
+    long long best = 0x7fffffff;
+    for (int b = 0; b < c->cfg.n_seq; ++b) {
+        const long long room = (long long)c->rows - (c->len[b] - c->base[b]);
+        best = std::min(best, room / T);
+    }
+    *steps = (int)std::max(0LL, best);
+    return KVQ_OK;
+}
+
+kvq_status kvq_physical_rows(const kvq_cache* c, int seq, int start, int end, int* phys_start, int* phys_end) {
+    if (!c || !phys_start || !phys_end) return fail(KVQ_EINVAL, "NULL argument");
+    if (seq < 0 || seq >= c->cfg.n_seq) return fail(KVQ_EINVAL, "sequence index out of range");
+    if (start < 0 || end < start) return fail(KVQ_ERANGE, "bad logical range");
+    const int base = c->base[seq];
+    if (start < base || end - base > c->rows)
+        return fail(KVQ_ERANGE, "logical rows [%d, %d) not resident (base %d, %d physical rows)", start, end, base,
+                    c->rows);
+    *phys_start = start - base;
+    *phys_end = end - base;
+    return KVQ_OK;
+}
+
+kvq_status kvq_read_device_error(kvq_cache* c, int* err, void* stream) {
+    if (!c || !err) return fail(KVQ_EINVAL, "NULL argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaMemcpy(err, c->err_d, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read error word");
+    e = cudaMemset(c->err_d, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+    return KVQ_OK;
+}
+
+kvq_status kvq_set_split_rows(kvq_cache* c, int rows) {
+    if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+    if (rows != 0 && (rows < kMinSplitRows || rows % 8))
+        return fail(KVQ_EINVAL, "split rows must be 0 or a multiple of 8 that is >= %d", kMinSplitRows);
+    c->split_rows = rows;
+    return KVQ_OK;
+}
+
+}  // extern "C"

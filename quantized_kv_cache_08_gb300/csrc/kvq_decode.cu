@@ -1,0 +1,731 @@
+// Split-K flash-decode attention over the quantised cache, and its merge.
+//
+// Semantics (cortiq-engine "Struct LayerKvCache", fn attend_group_upto and
+// fn o1_views; memra-engine "Struct KvLayer", fields len_d and base_d):
+//   query row t of a T-row step sits at position s0 + t (s0 = len - T) and
+//   sees logical rows [lstart_t, s0 + t + 1), lstart_t = max(0, s0+t+1-window)
+//   for a windowed cache, else 0; Q head h reads KV group h / hpk; the score
+//   is scale * <q, k_hat>; a sink logit joins the max and the denominator and
+//   carries no value; logical row r lives at physical row r - base.
+//
+// Work decomposition.  The visible rows of each sequence are cut into splits
+// of C rows; a work item is (sequence, split, query slice).  Persistent CTAs
+// (one per SM) take items blockIdx.x, +gridDim.x, ...; the split count of
+// every sequence comes from len_d on the device, so a captured launch replays
+// correctly as lengths grow.  A CTA covers all KV heads of its rows, so every
+// tile it stages is a contiguous byte range of each plane: one 1-D bulk TMA
+// copy (cp.async.bulk) per plane per tile of 16 token rows, completing on an
+// mbarrier, in a ring of `nstage` stages.
+//
+// Per tile:
+//   K phase  one thread per (query group of 4, KV head, 32-element block):
+//            32 int8 codes are turned into floats with a byte-permute into the
+//            mantissa of 2^23 and one packed subtract, then packed FMAs against
+//            the thread's 4 query vectors held in registers (pre-scaled by
+//            scale*log2 e); partial dots are scaled by the block's d and
+//            reduce-scattered over the head's blocks with warp shuffles.
+//   softmax  per query: tile max, lazy rescale (the reference maximum moves
+//            only when a score exceeds it by more than 8 in log2 units),
+//            p = 2^(s - m), running sum.
+//   V phase  one thread per (query group, KV head, block, half block): the
+//            5-bit codes are rebuilt from the nibbles and qh with byte
+//            arithmetic and placed into the mantissa of 0.5 (value 0.5+u/256),
+//            so v_hat = 256 d * F + (m - 128 d) and o += (p*256d) F by packed
+//            FMAs, with sum p*(m - 128 d) kept per block.
+// At the end of an item the V row groups are summed through shared memory and
+// the partial (max, sum, o[D]) of every query is written out; the merge
+// kernel combines the partials of a sequence with the sink by log-sum-exp.
+#include "kvq_internal.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace kvq {
+namespace {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kLazy = 8.0f;            // log2 units a score may exceed the reference max
+constexpr int kWaitIters = 1 << 22;      // bounded mbarrier wait
+
+// ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// bounded wait; false when it ran out
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (int i = 0; i < kWaitIters; ++i)
+        if (mbar_try(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ float load_q(const void* q, long long idx, int bf16) {
+    if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(q)[idx]);
+    return reinterpret_cast<const float*>(q)[idx];
+}
+
+__device__ __forceinline__ float h2f(uint32_t bits16) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
+}
+
+// ---------------------------------------------------------- work mapping
+
+struct Item {
+    int b, split, qs, pidx;
+};
+
+// visible-row window of sequence b for a T-row step: rows [lo, len)
+__device__ __forceinline__ void visible_rows(const SplitParams& p, int len, int& lo) {
+    lo = 0;
+    if (p.window > 0) lo = max(0, len - p.T + 1 - p.window);
+}
+
+__device__ __forceinline__ Item item_of(int idx, const int* prefix, int B, int nqs) {
+    Item it;
+    const int pi = idx / nqs;
+    it.qs = idx - pi * nqs;
+    int lo = 0, hi = B;  // largest b with prefix[b] <= pi
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= pi) lo = mid;
+        else hi = mid;
+    }
+    it.b = lo;
+    it.split = pi - prefix[lo];
+    it.pidx = pi;
+    return it;
+}
+
+// rows of the item: [row0, row0 + n), tiles of kTileRows
+struct ItemRows {
+    int row0, n, base, len;
+};
+
+__device__ __forceinline__ ItemRows item_rows(const SplitParams& p, const int* lens, const int* bases,
+                                              const Item& it) {
+    ItemRows r;
+    r.len = lens[it.b];
+    r.base = bases[it.b];
+    int lo;
+    visible_rows(p, r.len, lo);
+    r.row0 = lo + it.split * p.C;
+    r.n = min(p.C, r.len - r.row0);
+    return r;
+}
+
+// ------------------------------------------------------------ the kernel
+
+template <int NBH, int NQG>
+__global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitParams p) {
+    constexpr int QC = 4 * NQG;                    // queries per KV group per slice
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x;
+    const int Hkv = p.Hkv;
+    const int NQ = Hkv * QC;                       // CTA queries
+    const int nK = NQG * Hkv * NBH;                // K tasks per row
+    const int nV = 2 * nK;                         // V tasks per row
+    const int rpK = kSplitThreads / nK;            // rows per K pass
+    const int rpV = kSplitThreads / nV;            // rows per V pass
+
+    // ---- shared memory carve-up
+    uint8_t* stages = smem;
+    size_t off = (size_t)p.nstage * p.stage_bytes;
+    float* S = reinterpret_cast<float*>(smem + off);          // [2][kTileRows][NQ]
+    off += sizeof(float) * 2 * kTileRows * NQ;
+    float* m_run = reinterpret_cast<float*>(smem + off);
+    off += sizeof(float) * NQ;
+    float* l_run = reinterpret_cast<float*>(smem + off);
+    off += sizeof(float) * NQ;
+    float* alpha = reinterpret_cast<float*>(smem + off);
+    off += sizeof(float) * NQ;
+    float* red = reinterpret_cast<float*>(smem + off);        // [rpV-1][NQ][NBH*32]
+    off += sizeof(float) * (size_t)(rpV - 1) * NQ * NBH * 32;
+    int* lens = reinterpret_cast<int*>(smem + off);
+    off += sizeof(int) * p.B;
+    int* bases = reinterpret_cast<int*>(smem + off);
+    off += sizeof(int) * p.B;
+    int* prefix = reinterpret_cast<int*>(smem + off);         // [B+1]
+    off += sizeof(int) * (p.B + 1);
+    off = (off + 7) & ~size_t(7);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off);
+    __shared__ int s_abort;
+
+    // ---- plan: per-sequence split counts from the device lengths
+    for (int b = tid; b < p.B; b += kSplitThreads) {
+        lens[b] = p.len_d[b];
+        bases[b] = p.base_d[b];
+    }
+    if (tid == 0) s_abort = 0;
+    __syncthreads();
+    if (tid < 32) {
+        int carry = 0;
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const int b = b0 + tid;
+            int ns = 0;
+            if (b < p.B) {
+                const int len = lens[b];
+                int lo;
+                visible_rows(p, len, lo);
+                const bool bad = len < p.T || len - bases[b] > p.max_rows || lo < bases[b];
+                if (bad) {
+                    if (blockIdx.x == 0) atomicExch(p.err_d, kErrCounter);
+                } else {
+                    ns = (len - lo + p.C - 1) / p.C;
+                }
+            }
+            int x = ns;  // inclusive scan over the warp
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (tid >= o) x += y;
+            }
+            if (b < p.B) prefix[b] = carry + x - ns;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (tid == 0) prefix[p.B] = carry;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < p.nstage; ++s) mbar_init(smem_u32(&bars[s]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    for (int i = tid; i < NQ; i += kSplitThreads) {
+        m_run[i] = kNegInf;
+        l_run[i] = 0.f;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int b = tid; b <= p.B; b += kSplitThreads) p.plan[b] = prefix[b];
+    const int n_items = prefix[p.B] * p.nqs;
+    if ((int)blockIdx.x >= n_items) return;
+
+    // ---- producer state (thread 0 only): next tile to issue
+    int pr_item = blockIdx.x, pr_tile = 0;
+    int issued = 0;
+    auto issue_next = [&]() {
+        if (pr_item >= n_items) return;
+        const Item it = item_of(pr_item, prefix, p.B, p.nqs);
+        const ItemRows ir = item_rows(p, lens, bases, it);
+        const int r0 = ir.row0 + pr_tile * kTileRows;
+        const int nr = min(kTileRows, ir.row0 + ir.n - r0);
+        const int st = issued % p.nstage;
+        const uint32_t bar = smem_u32(&bars[st]);
+        const long long prow = (long long)it.b * p.max_rows + (r0 - ir.base);
+        const uint32_t kb = (uint32_t)nr * p.k_tok, vb = (uint32_t)nr * p.v_tok;
+        mbar_expect_tx(bar, kb + vb);
+        uint8_t* dst = stages + (size_t)st * p.stage_bytes;
+        bulk_g2s(smem_u32(dst), p.k_plane + prow * p.k_tok, kb, bar);
+        bulk_g2s(smem_u32(dst + p.k_stage_bytes), p.v_plane + prow * p.v_tok, vb, bar);
+        ++issued;
+        if (++pr_tile * kTileRows >= ir.n) {
+            pr_tile = 0;
+            pr_item += gridDim.x;
+        }
+    };
+    if (tid == 0)
+        for (int s = 0; s < p.nstage - 1; ++s) issue_next();
+
+    // ---- thread roles
+    // K task: (qg, g, bi) with bi fastest
+    const bool k_active = tid < rpK * nK;
+    const int k_rg = tid / nK, k_task = tid % nK;
+    const int k_bi = k_task % NBH, k_g = (k_task / NBH) % Hkv, k_qg = k_task / (NBH * Hkv);
+    const int k_blk = k_g * NBH + k_bi;
+    // V task: (qg, g, bi, half) with half fastest
+    const bool v_active = tid < rpV * nV;
+    const int v_rg = tid / nV, v_task = tid % nV;
+    const int v_hf = v_task & 1, v_bi = (v_task >> 1) % NBH, v_g = (v_task >> 1) / NBH % Hkv;
+    const int v_qg = (v_task >> 1) / (NBH * Hkv);
+    const int v_blk = v_g * NBH + v_bi;
+    const int v_qq0 = v_g * QC + 4 * v_qg;          // first of the thread's 4 CTA queries
+
+    float2 qv[4][16];                               // K thread: 4 queries x 32 dims
+    float2 o2[4][8];                                // V thread: 4 queries x 16 dims
+    float pm[4];                                    // V thread: sum p*(m - 128 d)
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+        pm[n] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o2[n][i] = make_float2(0.f, 0.f);
+    }
+
+    int tile_ctr = 0;                               // tiles consumed by this CTA
+    for (int item_idx = blockIdx.x; item_idx < n_items; item_idx += gridDim.x) {
+        const Item it = item_of(item_idx, prefix, p.B, p.nqs);
+        const ItemRows ir = item_rows(p, lens, bases, it);
+        const int s0 = ir.len - p.T;
+
+        // K thread: load its 4 query vectors (32 dims of block k_bi), pre-scaled
+        int kq_upto[4], kq_lo[4];
+        if (k_active) {
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                const int qi = it.qs * QC + 4 * k_qg + n;
+                const bool valid = qi < p.hpk * p.T;
+                const int t = valid ? qi / p.hpk : 0;
+                const int h = k_g * p.hpk + (valid ? qi % p.hpk : 0);
+                const long long base = ((long long)(it.b * p.T + t) * p.Hq + h) * p.D + k_bi * 32;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float a = 0.f, c = 0.f;
+                    if (valid) {
+                        a = load_q(p.q, base + 2 * i, p.q_bf16) * p.qscale;
+                        c = load_q(p.q, base + 2 * i + 1, p.q_bf16) * p.qscale;
+                    }
+                    qv[n][i] = make_float2(a, c);
+                }
+                const int upto = s0 + t + 1;
+                kq_upto[n] = valid ? upto : -1;     // invalid slot: no row visible
+                kq_lo[n] = p.window > 0 ? max(0, upto - p.window) : 0;
+            }
+        }
+
+        const int n_tiles = (ir.n + kTileRows - 1) / kTileRows;
+        for (int tl = 0; tl < n_tiles; ++tl, ++tile_ctr) {
+            const int st = tile_ctr % p.nstage;
+            const uint32_t sbase = smem_u32(stages + (size_t)st * p.stage_bytes);
+            const uint32_t ktile = sbase, vtile = sbase + p.k_stage_bytes;
+            const int r0 = ir.row0 + tl * kTileRows;
+            const int nr = min(kTileRows, ir.row0 + ir.n - r0);
+            float* Sb = S + (tile_ctr & 1) * kTileRows * NQ;
+
+            if (!mbar_wait(smem_u32(&bars[st]), (uint32_t)((tile_ctr / p.nstage) & 1))) {
+                atomicExch(p.err_d, kErrWait);
+                s_abort = 1;
+            }
+
+            // ------------------------------------------------ K phase
+            if (k_active) {
+                const int iters = (kTileRows + rpK - 1) / rpK;
+                for (int k = 0; k < iters; ++k) {
+                    const int r = k_rg + k * rpK;
+                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (r < nr) {
+                        const uint32_t a = ktile + (uint32_t)(r * p.k_tok + k_blk * kQ8Bytes);
+                        const uint32_t a0 = a & ~3u;
+                        const bool odd = (a & 2u) != 0;          // block starts at 2 mod 4
+                        uint32_t w[9];
+#pragma unroll
+                        for (int i = 0; i < 9; ++i) w[i] = lds32(a0 + 4 * i);
+                        const float d = h2f(odd ? (w[0] >> 16) : (w[0] & 0xffffu));
+                        const uint32_t sel = odd ? 0x7654u : 0x5432u;
+                        float2 acc[4];
+#pragma unroll
+                        for (int n = 0; n < 4; ++n) acc[n] = make_float2(0.f, 0.f);
+                        const float2 bias = make_float2(-8388736.f, -8388736.f);  // 2^23 + 128
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint32_t cw = __byte_perm(w[i], w[i + 1], sel) ^ 0x80808080u;
+                            const float2 f01 = __fadd2_rn(
+                                make_float2(__uint_as_float(__byte_perm(cw, 0x4B000000u, 0x7440u)),
+                                            __uint_as_float(__byte_perm(cw, 0x4B000000u, 0x7441u))),
+                                bias);
+                            const float2 f23 = __fadd2_rn(
+                                make_float2(__uint_as_float(__byte_perm(cw, 0x4B000000u, 0x7442u)),
+                                            __uint_as_float(__byte_perm(cw, 0x4B000000u, 0x7443u))),
+                                bias);
+#pragma unroll
+                            for (int n = 0; n < 4; ++n) {
+                                acc[n] = __ffma2_rn(qv[n][2 * i], f01, acc[n]);
+                                acc[n] = __ffma2_rn(qv[n][2 * i + 1], f23, acc[n]);
+                            }
+                        }
+#pragma unroll
+                        for (int n = 0; n < 4; ++n) sc[n] = (acc[n].x + acc[n].y) * d;
+                    }
+                    // reduce-scatter over the NBH blocks of the head (lanes k_bi)
+                    float res[4];
+                    int nres = 4, qsel0 = 0;
+                    if constexpr (NBH == 1) {
+#pragma unroll
+                        for (int n = 0; n < 4; ++n) res[n] = sc[n];
+                    } else {
+                        const unsigned FULL = 0xffffffffu;
+                        const int mA = NBH / 2;
+                        const bool hA = (k_bi & mA) != 0;
+                        const float s0a = hA ? sc[0] : sc[2], s1a = hA ? sc[1] : sc[3];
+                        const float k0a = hA ? sc[2] : sc[0], k1a = hA ? sc[3] : sc[1];
+                        const float w0 = k0a + __shfl_xor_sync(FULL, s0a, mA);
+                        const float w1 = k1a + __shfl_xor_sync(FULL, s1a, mA);
+                        qsel0 = hA ? 2 : 0;
+                        if constexpr (NBH == 2) {
+                            res[0] = w0;
+                            res[1] = w1;
+                            nres = 2;
+                        } else {
+                            const int mB = NBH / 4;
+                            const bool hB = (k_bi & mB) != 0;
+                            float x = (hB ? w1 : w0) + __shfl_xor_sync(FULL, hB ? w0 : w1, mB);
+#pragma unroll
+                            for (int m = NBH / 8; m >= 1; m >>= 1) x += __shfl_xor_sync(FULL, x, m);
+                            res[0] = x;
+                            nres = 1;
+                            qsel0 += hB ? 1 : 0;
+                        }
+                    }
+                    const bool writer = (NBH < 8) || ((k_bi & (NBH / 4 - 1)) == 0);
+                    if (r < nr && writer) {
+                        const int row = r0 + r;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (j < nres) {
+                                const int n = qsel0 + j;
+                                int lo_n = kq_lo[0], up_n = kq_upto[0];
+#pragma unroll
+                                for (int m2 = 1; m2 < 4; ++m2)
+                                    if (n == m2) {
+                                        lo_n = kq_lo[m2];
+                                        up_n = kq_upto[m2];
+                                    }
+                                const bool vis = row >= lo_n && row < up_n;
+                                Sb[r * NQ + k_g * QC + 4 * k_qg + n] = vis ? res[j] : kNegInf;
+                            }
+                        }
+                    }
+                }
+            }
+            // invalid rows of a partial tile
+            if (nr < kTileRows)
+                for (int i = tid; i < (kTileRows - nr) * NQ; i += kSplitThreads) Sb[nr * NQ + i] = kNegInf;
+            __syncthreads();                                        // (A)
+            if (s_abort) break;
+            if (tid == 0) issue_next();                             // stage of the previous tile is free
+
+            // ------------------------------------------------ online softmax
+            for (int qq0 = 0; qq0 < NQ; qq0 += kSplitThreads / kTileRows) {
+                const int qq = qq0 + tid / kTileRows;
+                const int r = tid % kTileRows;
+                const bool act = qq < NQ;
+                const float s = act ? Sb[r * NQ + qq] : kNegInf;
+                float tmax = s;
+#pragma unroll
+                for (int o = kTileRows / 2; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+                const float mo = act ? m_run[qq] : kNegInf;
+                float mn = mo, al = 1.f;
+                if (tmax > mo + kLazy || (mo == kNegInf && tmax != kNegInf)) {
+                    mn = tmax;
+                    al = (mo == kNegInf) ? 0.f : exp2f(mo - mn);
+                }
+                const float pv = (s == kNegInf) ? 0.f : exp2f(s - mn);
+                float sum = pv;
+#pragma unroll
+                for (int o = kTileRows / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                if (act) {
+                    Sb[r * NQ + qq] = pv;
+                    if (r == 0) {
+                        m_run[qq] = mn;
+                        l_run[qq] = l_run[qq] * al + sum;
+                        alpha[qq] = al;
+                    }
+                }
+            }
+            __syncthreads();                                        // (B)
+
+            // ------------------------------------------------ V phase
+            if (v_active) {
+                const float4 al4 = *reinterpret_cast<const float4*>(&alpha[v_qq0]);
+                const float alv[4] = {al4.x, al4.y, al4.z, al4.w};
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    if (alv[n] != 1.f) {
+                        pm[n] *= alv[n];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            o2[n][i].x *= alv[n];
+                            o2[n][i].y *= alv[n];
+                        }
+                    }
+                }
+                const uint32_t sb = smem_u32(Sb);
+                for (int r = v_rg; r < nr; r += rpV) {
+                    const uint32_t vb = vtile + (uint32_t)(r * p.v_tok + v_blk * kQ5Bytes);
+                    const uint2 dmqh = lds64(vb);
+                    const uint2 qs = lds64(vb + 8 + 8 * v_hf);
+                    const float4 p4 = lds128f(sb + 4u * (uint32_t)(r * NQ + v_qq0));
+                    const float d = h2f(dmqh.x & 0xffffu);
+                    const float m = h2f(dmqh.x >> 16);
+                    const float d256 = d * 256.f;
+                    const float mp = fmaf(-128.f, d, m);
+                    const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
+                    float2 pd[4];
+#pragma unroll
+                    for (int n = 0; n < 4; ++n) {
+                        const float t = pr[n] * d256;
+                        pd[n] = make_float2(t, t);
+                        pm[n] = fmaf(pr[n], mp, pm[n]);
+                    }
+                    // 5-bit codes: nibbles from qs, bit 4 from qh
+                    const uint32_t xl = __byte_perm(dmqh.y, 0, v_hf ? 0x1111u : 0x0000u);  // qh byte for dims lo
+                    const uint32_t xh = __byte_perm(dmqh.y, 0, v_hf ? 0x3333u : 0x2222u);  // qh byte for dims +16
+                    uint32_t u[4];
+                    {
+                        const uint32_t sp0 = ((xl & 0x08040201u) + 0x080C0E0Fu);
+                        const uint32_t sp1 = (((xl >> 4) & 0x08040201u) + 0x080C0E0Fu);
+                        const uint32_t sp2 = ((xh & 0x08040201u) + 0x080C0E0Fu);
+                        const uint32_t sp3 = (((xh >> 4) & 0x08040201u) + 0x080C0E0Fu);
+                        u[0] = (qs.x & 0x0F0F0F0Fu) | (sp0 & 0xF0F0F0F0u);          // dims j0..j0+3
+                        u[1] = (qs.y & 0x0F0F0F0Fu) | (sp1 & 0xF0F0F0F0u);          // dims j0+4..j0+7
+                        u[2] = ((qs.x >> 4) & 0x0F0F0F0Fu) | (sp2 & 0xF0F0F0F0u);   // dims j0+16..
+                        u[3] = ((qs.y >> 4) & 0x0F0F0F0Fu) | (sp3 & 0xF0F0F0F0u);   // dims j0+20..
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float2 fa = make_float2(__uint_as_float(__byte_perm(u[c], 0x3F000000u, 0x7044u)),
+                                                      __uint_as_float(__byte_perm(u[c], 0x3F000000u, 0x7144u)));
+                        const float2 fb = make_float2(__uint_as_float(__byte_perm(u[c], 0x3F000000u, 0x7244u)),
+                                                      __uint_as_float(__byte_perm(u[c], 0x3F000000u, 0x7344u)));
+#pragma unroll
+                        for (int n = 0; n < 4; ++n) {
+                            o2[n][2 * c] = __ffma2_rn(pd[n], fa, o2[n][2 * c]);
+                            o2[n][2 * c + 1] = __ffma2_rn(pd[n], fb, o2[n][2 * c + 1]);
+                        }
+                    }
+                }
+            }
+        }
+        if (s_abort) break;
+
+        // ---------------------------------------------------- finalize item
+        __syncthreads();                                            // (C)
+        const int Dh = NBH * 32;
+        // thread dims: c in 0..3 covers 4 dims: base j0 = 8*hf (+4 for c odd, +16 for c >= 2)
+        if (v_active && v_rg > 0) {
+            float* dst = red + (size_t)(v_rg - 1) * NQ * Dh;
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                const int qq = v_qq0 + n;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int dim = v_bi * 32 + 8 * v_hf + (c & 1) * 4 + (c >> 1) * 16;
+                    float4 val = make_float4(o2[n][2 * c].x + pm[n], o2[n][2 * c].y + pm[n],
+                                             o2[n][2 * c + 1].x + pm[n], o2[n][2 * c + 1].y + pm[n]);
+                    *reinterpret_cast<float4*>(&dst[(size_t)qq * Dh + dim]) = val;
+                }
+            }
+        }
+        __syncthreads();                                            // (D)
+        if (v_active && v_rg == 0) {
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                const int qq = v_qq0 + n;
+                const int qi = it.qs * QC + 4 * v_qg + n;
+                const bool valid = qi < p.hpk * p.T;
+                const int t = valid ? qi / p.hpk : 0;
+                const int h = v_g * p.hpk + (valid ? qi % p.hpk : 0);
+                const long long rec = (long long)it.pidx * p.Qtot + (long long)t * p.Hq + h;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int dim = v_bi * 32 + 8 * v_hf + (c & 1) * 4 + (c >> 1) * 16;
+                    float4 val = make_float4(o2[n][2 * c].x + pm[n], o2[n][2 * c].y + pm[n],
+                                             o2[n][2 * c + 1].x + pm[n], o2[n][2 * c + 1].y + pm[n]);
+                    for (int g2 = 0; g2 < rpV - 1; ++g2) {
+                        const float4 o = *reinterpret_cast<const float4*>(&red[((size_t)g2 * NQ + qq) * Dh + dim]);
+                        val.x += o.x;
+                        val.y += o.y;
+                        val.z += o.z;
+                        val.w += o.w;
+                    }
+                    if (valid) *reinterpret_cast<float4*>(&p.part_o[rec * p.D + dim]) = val;
+                }
+                if (valid && v_bi == 0 && v_hf == 0) {
+                    p.part_ml[rec * 2] = m_run[qq];
+                    p.part_ml[rec * 2 + 1] = l_run[qq];
+                }
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            pm[n] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o2[n][i] = make_float2(0.f, 0.f);
+        }
+        __syncthreads();                                            // (E)
+        for (int i = tid; i < NQ; i += kSplitThreads) {
+            m_run[i] = kNegInf;
+            l_run[i] = 0.f;
+        }
+        // the next item's first tile writes S only after its K phase; m_run
+        // is read after barrier (A), which orders this reset before it
+    }
+
+    if (s_abort && tid == 0) {
+        // drain copies still in flight into this CTA's shared memory
+        for (int s = 0; s < p.nstage; ++s) mbar_wait(smem_u32(&bars[s]), 0), mbar_wait(smem_u32(&bars[s]), 1);
+    }
+}
+
+// Merge the partials of one (sequence, query) over its splits, with the sink:
+// M = max(sink, m_s), L = 2^(sink-M) + sum l_s 2^(m_s-M), out = sum o_s 2^(m_s-M) / L
+// (all in log2 units).  CTA = (query record, sequence, 32-dim chunk); warps
+// stride over splits, lanes over dims.
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+    extern __shared__ float wsh[];                  // [max_splits] weights, then [8][32] partial sums
+    const int gq = blockIdx.x;                      // t * Hq + h
+    const int b = blockIdx.y;
+    const int dchunk = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int first = p.plan[b];
+    const int ns = p.plan[b + 1] - first;
+    const int h = gq % p.Hq;
+    const float LOG2E = 1.4426950408889634f;
+    const float sink = p.sinks ? p.sinks[h] * LOG2E : kNegInf;
+    __shared__ float red[kMergeThreads / 32];
+    __shared__ float s_M, s_L;
+    // max
+    float mx = sink;
+    for (int s = tid; s < ns; s += kMergeThreads)
+        mx = fmaxf(mx, p.part_ml[((long long)(first + s) * p.Qtot + gq) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        float m = red[0];
+        for (int i = 1; i < kMergeThreads / 32; ++i) m = fmaxf(m, red[i]);
+        s_M = m;
+    }
+    __syncthreads();
+    const float M = s_M;
+    float* w = wsh;
+    float lsum = 0.f;
+    for (int s = tid; s < ns; s += kMergeThreads) {
+        const long long rec = ((long long)(first + s) * p.Qtot + gq) * 2;
+        const float ms = p.part_ml[rec];
+        const float ws = (ms == kNegInf) ? 0.f : exp2f(ms - M);
+        w[s] = ws;
+        lsum += ws * p.part_ml[rec + 1];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = lsum;
+    __syncthreads();
+    if (tid == 0) {
+        float l = (sink == kNegInf) ? 0.f : exp2f(sink - M);
+        for (int i = 0; i < kMergeThreads / 32; ++i) l += red[i];
+        s_L = l;
+    }
+    __syncthreads();
+    const int dim = dchunk * 32 + lane;
+    float acc = 0.f;
+    for (int s = warp; s < ns; s += kMergeThreads / 32)
+        acc += w[s] * p.part_o[((long long)(first + s) * p.Qtot + gq) * p.D + dim];
+    float* part = wsh + ((ns + 31) & ~31);
+    part[warp * 32 + lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        float tot = 0.f;
+        for (int i = 0; i < kMergeThreads / 32; ++i) tot += part[i * 32 + lane];
+        p.out[(((long long)b * p.Qtot) + gq) * p.D + dim] = tot / s_L;
+    }
+}
+
+template <int NBH, int NQG>
+cudaError_t launch_split_t(const SplitParams& p, int grid, size_t smem, cudaStream_t s) {
+    auto fn = split_kernel<NBH, NQG>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    fn<<<grid, kSplitThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t split_smem_bytes(const SplitParams& p) {
+    const int NQ = p.Hkv * p.QC;
+    const int NBH = p.D / 32;
+    const int nV = 2 * (p.QC / 4) * p.Hkv * NBH;
+    const int rpV = kSplitThreads / nV;
+    size_t off = (size_t)p.nstage * p.stage_bytes;
+    off += sizeof(float) * 2 * kTileRows * NQ;
+    off += sizeof(float) * 3 * NQ;
+    off += sizeof(float) * (size_t)(rpV - 1) * NQ * p.D;
+    off += sizeof(int) * (3 * (size_t)p.B + 1);
+    off = (off + 7) & ~size_t(7);
+    off += 8 * (size_t)p.nstage;
+    return off;
+}
+
+int split_max_smem() {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    return v - 1024;  // static shared variables
+}
+
+cudaError_t launch_split(const SplitParams& p, int grid, cudaStream_t s) {
+    const size_t smem = split_smem_bytes(p);
+    const int NBH = p.D / 32, NQG = p.QC / 4;
+#define KVQ_CASE(nb, nq) \
+    if (NBH == nb && NQG == nq) return launch_split_t<nb, nq>(p, grid, smem, s);
+    KVQ_CASE(1, 1) KVQ_CASE(2, 1) KVQ_CASE(4, 1) KVQ_CASE(8, 1) KVQ_CASE(16, 1)
+    KVQ_CASE(1, 2) KVQ_CASE(2, 2) KVQ_CASE(4, 2) KVQ_CASE(8, 2) KVQ_CASE(16, 2)
+#undef KVQ_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_merge(const MergeParams& p, int T, int max_splits, bool pdl, cudaStream_t s) {
+    const size_t smem = sizeof(float) * ((size_t)((max_splits + 31) & ~31) + kMergeThreads);
+    cudaError_t e = cudaSuccess;
+    if (smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.Hq * T), (unsigned)p.B, (unsigned)(p.D / 32));
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, merge_kernel, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,333 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Append bytes must be bit-exact; attention outputs must be within 2e-3 max abs
+error of the oracle run on the same quantised bytes.  Small cases span several
+16-row tiles, several splits and ragged tails; edge cases cover exact rounding
+ties, adversarial scales, constant blocks, bf16 inputs, partial sequence
+subsets, windows, rings, sinks and T-row causal steps."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvq_oracle as O
+from tests.kvq_testutil import ATOL, Pair, assert_close, assert_rows_equal, need_gpu, to_dev
+from quantized_kv_cache_08_gb300 import _binding as B
+from quantized_kv_cache_08_gb300.cache import KVCache
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _randn(*shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(*shape, generator=g) * scale
+
+
+# ------------------------------------------------------------------ append
+
+@pytest.mark.parametrize("n_kv,D,T,dtype", [
+    (2, 128, 1, torch.float32), (2, 128, 7, torch.float32), (8, 64, 3, torch.float32),
+    (1, 32, 5, torch.float32), (4, 256, 2, torch.bfloat16), (3, 96, 4, torch.float32),
+])
+def test_append_bytes_exact(n_kv, D, T, dtype):
+    B_ = 3
+    p = Pair(B_, n_kv, D, n_kv * 2, max_t=T, max_rows=64)
+    for step in range(4):
+        k = _randn(B_, T, n_kv, D, seed=10 * step + 1, scale=3.0).to(dtype)
+        v = _randn(B_, T, n_kv, D, seed=10 * step + 2, scale=0.5).to(dtype) + 1.0
+        p.append(k, v)
+    # a subset of sequences, in a permuted order
+    k = _randn(2, T, n_kv, D, seed=99).to(dtype)
+    p.append(k, -k, seq_ids=[2, 0])
+    assert p.dev.lens() == [5 * T, 4 * T, 5 * T]
+    for b in range(B_):
+        assert_rows_equal(p.dev, p.ora, b, 0, p.dev.lens()[b])
+    assert p.dev.device_error() == 0
+
+
+def test_append_rounding_edge_cases():
+    """Exact ties, adversarial scales, constant and zero blocks, tiny values."""
+    n_kv, D = 1, 32
+    rows = []
+    # q8_0: amax = 127 -> d = 1, halves go away from zero
+    r = np.zeros(32, np.float32)
+    r[0] = 127
+    r[1:] = np.arange(31) - 15 + 0.5
+    rows.append(r)
+    # q8_0 scale on an fp16 midpoint +-1 ulp: amax = 127 * midpoint
+    for bits in (0x3C00, 0x2E66, 0x0400, 0x1234):
+        lo = np.array(bits, np.uint16).view(np.float16).astype(np.float64)
+        hi = np.array(bits + 1, np.uint16).view(np.float16).astype(np.float64)
+        a = np.float32(127.0 * (lo + hi) / 2)
+        for x in (a, np.nextafter(a, np.float32(0)), np.nextafter(a, np.float32(np.inf))):
+            r = np.linspace(-1, 1, 32).astype(np.float32) * x * np.float32(0.9)
+            r[7] = x
+            rows.append(r)
+    # code ties for d = 0.5: multiples of 0.25
+    rows.append((np.arange(32, dtype=np.float32) - 16) * np.float32(0.25) + np.float32(0.0))
+    # constant block (q5_1 d = 0), zero block, tiny values (subnormal fp16 scale)
+    rows.append(np.full(32, 0.3, np.float32))
+    rows.append(np.zeros(32, np.float32))
+    rows.append((np.arange(32, dtype=np.float32) - 16) * np.float32(1e-6))
+    # q5_1 ties: min 0, max 31 -> d = 1, values at n + 0.5
+    rows.append(np.concatenate([[0.0, 31.0], np.arange(30) + 0.5]).astype(np.float32))
+    # large magnitudes
+    rows.append(np.linspace(-6e4, 6e4, 32).astype(np.float32))
+    x = torch.from_numpy(np.stack(rows)).view(len(rows), 1, n_kv, D)
+    p = Pair(len(rows), n_kv, D, 1, max_rows=4)
+    p.append(x, x)
+    for b in range(len(rows)):
+        assert_rows_equal(p.dev, p.ora, b, 0, 1)
+
+
+def test_append_t512_equals_512_single_rows():
+    """One T=512 append and 512 T=1 appends write identical bytes."""
+    from quantized_kv_cache_08_gb300.inputs import workload
+    wl = workload("ctx512")
+    k, v = wl.kv(0, 0, 512)
+    a = KVCache(1, wl.n_kv, wl.head_dim, wl.n_q, max_t=64, max_rows=512)
+    b = KVCache(1, wl.n_kv, wl.head_dim, wl.n_q, max_t=64, max_rows=512)
+    kd, vd = to_dev(k), to_dev(v)
+    for t0 in range(0, 512, 64):           # max_t caps one call at 64 rows
+        a.append(kd[t0:t0 + 64].unsqueeze(0), vd[t0:t0 + 64].unsqueeze(0))
+    for t in range(512):
+        b.append(kd[t:t + 1].unsqueeze(0), vd[t:t + 1].unsqueeze(0))
+    assert torch.equal(a.k_plane, b.k_plane) and torch.equal(a.v_plane, b.v_plane)
+    ora = O.OracleKvCache(1, wl.n_kv, wl.head_dim)
+    ora.append(k.unsqueeze(0).numpy(), v.unsqueeze(0).numpy())
+    assert_rows_equal(a, ora, 0, 0, 512)
+
+
+# ------------------------------------------------------------------ decode
+
+CASES = [
+    # B, Hq, Hkv, D, lens, T, window, ring, sinks, qdtype
+    (1, 8, 2, 128, [512], 1, 0, False, False, torch.float32),
+    (1, 8, 2, 128, [37], 1, 0, False, False, torch.float32),
+    (3, 32, 8, 128, [1000, 1, 333], 1, 0, False, False, torch.float32),
+    (2, 32, 8, 128, [700, 2049], 1, 0, False, True, torch.bfloat16),
+    (1, 64, 8, 64, [600], 1, 128, False, True, torch.float32),
+    (1, 16, 4, 256, [500], 8, 0, False, False, torch.float32),
+    (2, 16, 4, 256, [300, 77], 8, 50, False, True, torch.float32),
+    (1, 8, 8, 32, [90], 1, 0, False, False, torch.float32),
+    (2, 16, 8, 32, [130, 64], 3, 0, False, True, torch.float32),
+    (1, 32, 8, 64, [257], 2, 0, False, False, torch.float32),
+    (4, 8, 2, 128, [5, 17, 64, 65], 4, 0, False, True, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
+def test_decode_matches_oracle(case):
+    Bn, Hq, Hkv, D, lens, T, window, ring, sinks, qdt = case
+    p = Pair(Bn, Hkv, D, Hq, max_t=max(T, 64), max_rows=max(lens) + T, window=window, ring=ring)
+    for b, L in enumerate(lens):
+        k = _randn(1, L, Hkv, D, seed=100 + b)
+        v = _randn(1, L, Hkv, D, seed=200 + b)
+        for t0 in range(0, L, 64):
+            p.append(k[:, t0:t0 + 64], v[:, t0:t0 + 64], seq_ids=[b])
+    q = _randn(Bn, T, Hq, D, seed=7).to(qdt)
+    s = _randn(Hq, seed=8) if sinks else None
+    got, ref = p.decode(q, sinks=s)
+    assert_close(got, ref)
+    assert p.dev.device_error() == 0
+
+
+@pytest.mark.parametrize("split_rows", [64, 72, 128, 1000, 4096])
+def test_decode_split_sizes_agree(split_rows):
+    Hq, Hkv, D, L = 32, 8, 128, 3000
+    p = Pair(2, Hkv, D, Hq, max_t=64, max_rows=L)
+    for b in range(2):
+        k = _randn(1, L - 100 * b, Hkv, D, seed=300 + b)
+        for t0 in range(0, k.shape[1], 64):
+            p.append(k[:, t0:t0 + 64], 0.5 * k[:, t0:t0 + 64], seq_ids=[b])
+    p.dev.set_split_rows(split_rows)
+    q = _randn(2, 1, Hq, D, seed=9)
+    got, ref = p.decode(q)
+    assert_close(got, ref)
+
+
+def test_decode_scale_override_and_outlier_scores():
+    Hq, Hkv, D, L = 8, 2, 64, 400
+    p = Pair(1, Hkv, D, Hq, max_t=64, max_rows=L)
+    k = _randn(1, L, Hkv, D, seed=41, scale=4.0)
+    for t0 in range(0, L, 64):
+        p.append(k[:, t0:t0 + 64], k[:, t0:t0 + 64] * 0.1, seq_ids=[0])
+    q = _randn(1, 1, Hq, D, seed=42, scale=3.0)
+    got, ref = p.decode(q, scale=0.3)
+    assert_close(got, ref)
+
+
+# -------------------------------------------------- invariants on the GPU
+
+def test_gqa_equals_repeated_kv_heads_on_gpu():
+    Hq, Hkv, D, L = 16, 2, 128, 700
+    hpk = Hq // Hkv
+    k = _randn(1, L, Hkv, D, seed=51)
+    v = _randn(1, L, Hkv, D, seed=52)
+    q = _randn(1, 1, Hq, D, seed=53)
+    a = KVCache(1, Hkv, D, Hq, max_t=64, max_rows=L)
+    r = KVCache(1, Hq, D, Hq, max_t=64, max_rows=L)
+    kr = k.repeat_interleave(hpk, dim=2)
+    vr = v.repeat_interleave(hpk, dim=2)
+    for t0 in range(0, L, 64):
+        a.append(to_dev(k[:, t0:t0 + 64]), to_dev(v[:, t0:t0 + 64]))
+        r.append(to_dev(kr[:, t0:t0 + 64]), to_dev(vr[:, t0:t0 + 64]))
+    oa = a.decode(to_dev(q)).cpu().numpy()
+    orr = r.decode(to_dev(q)).cpu().numpy()
+    assert np.max(np.abs(oa - orr)) <= 1e-5
+
+
+def test_window_covering_len_equals_full_and_neg_inf_sink_equals_plain():
+    Hq, Hkv, D, L = 8, 2, 128, 300
+    k = _randn(1, L, Hkv, D, seed=61)
+    v = _randn(1, L, Hkv, D, seed=62)
+    q = to_dev(_randn(1, 1, Hq, D, seed=63))
+    full = KVCache(1, Hkv, D, Hq, max_t=64, max_rows=L)
+    win = KVCache(1, Hkv, D, Hq, max_t=64, max_rows=L, window=L)
+    for t0 in range(0, L, 64):
+        for c in (full, win):
+            c.append(to_dev(k[:, t0:t0 + 64]), to_dev(v[:, t0:t0 + 64]))
+    o_full = full.decode(q)
+    o_win = win.decode(q)
+    o_sink = full.decode(q, sinks=torch.full((Hq,), -math.inf, device="cuda"))
+    assert torch.max(torch.abs(o_full - o_win)).item() <= 1e-6
+    assert torch.max(torch.abs(o_full - o_sink)).item() <= 1e-6
+
+
+def test_causal_rows_equal_sequential_decodes():
+    Hq, Hkv, D, L0, T = 16, 4, 128, 400, 8
+    k = _randn(1, L0 + T, Hkv, D, seed=71)
+    v = _randn(1, L0 + T, Hkv, D, seed=72)
+    q = _randn(1, T, Hq, D, seed=73)
+    par = KVCache(1, Hkv, D, Hq, max_t=64, max_rows=L0 + T, window=100)
+    seq = KVCache(1, Hkv, D, Hq, max_t=64, max_rows=L0 + T, window=100)
+    for t0 in range(0, L0, 64):
+        t1 = min(L0, t0 + 64)
+        for c in (par, seq):
+            c.append(to_dev(k[:, t0:t1]), to_dev(v[:, t0:t1]))
+    par.append(to_dev(k[:, L0:]), to_dev(v[:, L0:]))
+    o_par = par.decode(to_dev(q)).cpu()
+    for t in range(T):
+        seq.append(to_dev(k[:, L0 + t:L0 + t + 1]), to_dev(v[:, L0 + t:L0 + t + 1]))
+        o_t = seq.decode(to_dev(q[:, t:t + 1])).cpu()
+        assert torch.max(torch.abs(o_t[0, 0] - o_par[0, t])).item() <= 1e-5
+
+
+# ----------------------------------------------------- truncate and ring
+
+def test_truncate_then_reappend_equals_clean_build():
+    Hkv, D, Hq = 4, 64, 8
+    p = Pair(2, Hkv, D, Hq, max_t=8, max_rows=80)
+    k = _randn(2, 40, Hkv, D, seed=81)
+    junk = _randn(2, 8, Hkv, D, seed=82)
+    for t0 in range(0, 40, 8):
+        p.append(k[:, t0:t0 + 8], -k[:, t0:t0 + 8])
+    p.append(junk, junk)
+    p.truncate([43, 40])
+    assert p.dev.lens() == [43, 40]
+    p.append(k[:, :8], k[:, :8])
+    for b in range(2):
+        assert_rows_equal(p.dev, p.ora, b, 0, p.dev.lens()[b])
+    got, ref = p.decode(_randn(2, 1, Hq, D, seed=83))
+    assert_close(got, ref)
+    with pytest.raises(B.KvqError) as e:
+        p.truncate([100, 0])
+    assert e.value.status == B.KVQ_ERANGE
+
+
+def test_ring_growth_matches_flat_oracle_and_keeps_invariants():
+    """A small ring (window 64 + 31 rows) grown to 600 rows, T=1 steps: the
+    live rows equal the oracle's logical rows, at most 31 masked rows precede
+    the window, and outputs match the windowed oracle at every step."""
+    Hq, Hkv, D, W, N = 16, 2, 64, 64, 600
+    p = Pair(1, Hkv, D, Hq, max_t=1, window=W, ring=True)
+    assert p.dev.rows == W + 31
+    k = _randn(1, N, Hkv, D, seed=91)
+    v = _randn(1, N, Hkv, D, seed=92)
+    s = _randn(Hq, seed=93)
+    for t in range(N):
+        p.append(k[:, t:t + 1], v[:, t:t + 1])
+        L = t + 1
+        base = p.dev.bases()[0]
+        lstart = max(0, L - W)
+        assert lstart - base <= 31 and L - base <= p.dev.rows
+        if t % 7 == 0 or t < 70 or t > N - 3:
+            got, ref = p.decode(_randn(1, 1, Hq, D, seed=1000 + t), sinks=s)
+            assert_close(got, ref, what=f"step {t}")
+            assert_rows_equal(p.dev, p.ora, 0, max(base, lstart), L)
+    # rewinds never move base; truncating into rows the ring dropped fails
+    base = p.dev.bases()[0]
+    p.truncate([N - 5])
+    assert p.dev.bases()[0] == base
+    with pytest.raises(B.KvqError) as e:
+        p.dev.truncate([base + W - 10])
+    assert e.value.status == B.KVQ_ERANGE
+    got, ref = p.decode(_randn(1, 1, Hq, D, seed=5000), sinks=s)
+    assert_close(got, ref)
+
+
+def test_flat_capacity_errors_enqueue_nothing():
+    c = KVCache(1, 2, 64, 4, max_t=4, max_rows=6)
+    x = torch.zeros(1, 4, 2, 64, device="cuda")
+    c.append(x, x)
+    with pytest.raises(B.KvqError) as e:
+        c.append(x, x)
+    assert e.value.status == B.KVQ_ERANGE
+    assert c.lens() == [4]
+    with pytest.raises(B.KvqError) as e:
+        c.decode(torch.zeros(1, 5, 4, 64, device="cuda"))
+    assert e.value.status == B.KVQ_EINVAL      # T above max_t
+    assert c.device_error() == 0
+
+
+# ------------------------------------------------------------ graph capture
+
+def test_captured_append_decode_replays_as_lengths_grow():
+    Hq, Hkv, D, L0, steps = 32, 8, 128, 1000, 24
+    p = Pair(1, Hkv, D, Hq, max_t=64, max_rows=L0 + steps + 1)
+    k = _randn(1, L0 + steps + 1, Hkv, D, seed=101)
+    v = _randn(1, L0 + steps + 1, Hkv, D, seed=102)
+    for t0 in range(0, L0, 64):
+        p.append(k[:, t0:min(L0, t0 + 64)], v[:, t0:min(L0, t0 + 64)])
+    kd, vd = to_dev(k), to_dev(v)
+    k_in = torch.empty(1, 1, Hkv, D, device="cuda")
+    v_in = torch.empty_like(k_in)
+    q_in = torch.empty(1, 1, Hq, D, device="cuda")
+    out = torch.empty(1, 1, Hq, D, device="cuda")
+    # warm up once outside the capture (sets kernel attributes), then roll back
+    k_in.copy_(kd[:, L0:L0 + 1])
+    v_in.copy_(vd[:, L0:L0 + 1])
+    p.dev.append(k_in, v_in)
+    p.dev.decode(q_in, out=out)
+    p.dev.truncate([L0])
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        p.dev.append(k_in, v_in)
+        p.dev.decode(q_in, out=out)
+    # capture enqueued but did not run the append: roll the host mirror back
+    p.dev.note_replayed(0, 1)
+    lens_after_capture = p.dev.lens()[0]
+    p.dev.truncate([L0])
+    assert lens_after_capture == L0 + 1
+    for t in range(steps):
+        q = _randn(1, 1, Hq, D, seed=2000 + t)
+        k_in.copy_(kd[:, L0 + t:L0 + t + 1])
+        v_in.copy_(vd[:, L0 + t:L0 + t + 1])
+        q_in.copy_(to_dev(q))
+        g.replay()
+        p.dev.note_replayed(1, 1)
+        p.ora.append(k[:, L0 + t:L0 + t + 1].numpy(), v[:, L0 + t:L0 + t + 1].numpy())
+        torch.cuda.synchronize()
+        ref = p.ora.decode(q.double().numpy())
+        assert_close(out.cpu().numpy(), ref, what=f"replay {t}")
+    assert p.dev.lens() == [L0 + steps]
+    assert_rows_equal(p.dev, p.ora, 0, 0, L0 + steps)
