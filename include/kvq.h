@@ -91,8 +91,9 @@ typedef struct kvq_config {
 } kvq_config;
 
 /* Device bytes the caller provides (each buffer 16-byte aligned):
- *   k_plane   [n_seq][max_rows][kb*34]  kb = n_kv_heads*head_dim/32
- *   v_plane   [n_seq][max_rows][kb*24]
+ *   k_plane   [n_seq][max_rows][kb*34]  kb = n_kv_heads*head_dim/32, size
+ *             rounded up to a multiple of 256 bytes
+ *   v_plane   [n_seq][max_rows][kb*24]  (likewise rounded up)
  *   counters  len_d[n_seq], base_d[n_seq], error word (int32)
  *   workspace decode partials, the split plan and the ring-rebase scratch   */
 typedef struct kvq_sizes {
@@ -174,6 +175,17 @@ kvq_status kvq_physical_rows(const kvq_cache* cache, int seq, int start,
  * 1 = a kernel saw a length or base out of range; 2 = a bounded wait ran
  * out) and clear it. */
 kvq_status kvq_read_device_error(kvq_cache* cache, int* err, void* stream);
+
+/* Choose the decode kernel: path 0 = automatic (the warp-specialised kernel
+ * whenever token rows are 16-byte multiples and its tiles fit shared memory,
+ * else the generic split kernel), 1 = generic, 2 = warp-specialised
+ * (KVQ_EUNSUPPORTED at decode time if the geometry does not allow it).
+ * query_bits (0 = 24, or 16): the warp-specialised kernel quantises each
+ * pre-scaled query element per 32-element block to this many bits against
+ * the block's largest magnitude and multiplies with int8 dot products; 24
+ * bits is at the level of fp32 rounding, 16 bits adds an error below 1e-4
+ * to the attention output on unit-variance data. */
+kvq_status kvq_set_decode_path(kvq_cache* cache, int path, int query_bits);
 
 /* Override the decode split size in rows (a multiple of 8, >= 64; 0 = auto). */
 kvq_status kvq_set_split_rows(kvq_cache* cache, int rows);

@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ERANGE", 3: "KVQ_ECUDA", 4
 EXPORTS = (
     "kvq_required_bytes", "kvq_alloc", "kvq_free", "kvq_append", "kvq_decode",
     "kvq_truncate", "kvq_get_len", "kvq_note_replayed", "kvq_ring_headroom",
-    "kvq_physical_rows", "kvq_read_device_error", "kvq_set_split_rows",
+    "kvq_physical_rows", "kvq_read_device_error", "kvq_set_split_rows", "kvq_set_decode_path",
     "kvq_block_bytes", "kvq_bytes_per_token", "kvq_last_error",
 )
 
@@ -76,6 +76,7 @@ def lib():
             "kvq_physical_rows": (I, [P, I, I, I, IP, IP]),
             "kvq_read_device_error": (I, [P, IP, P]),
             "kvq_set_split_rows": (I, [P, I]),
+            "kvq_set_decode_path": (I, [P, I, I]),
             "kvq_block_bytes": (I, [I]),
             "kvq_bytes_per_token": (S, [ctypes.POINTER(kvq_config)]),
             "kvq_last_error": (ctypes.c_char_p, []),
@@ -167,6 +168,10 @@ def kvq_read_device_error(handle, stream=0):
 
 def kvq_set_split_rows(handle, rows):
     _check(lib().kvq_set_split_rows(handle, rows))
+
+
+def kvq_set_decode_path(handle, path, query_bits=0):
+    _check(lib().kvq_set_decode_path(handle, path, query_bits))
 
 
 def kvq_block_bytes(fmt):

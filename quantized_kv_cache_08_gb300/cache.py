@@ -49,7 +49,10 @@ class KVCache:
         self.n_seq, self.n_kv_heads, self.head_dim = n_seq, n_kv_heads, head_dim
         kb = n_kv_heads * head_dim // 32
         self.k_tok, self.v_tok = kb * 34, kb * 24
-        self.rows = sz.k_plane // (n_seq * self.k_tok)
+        if ring:
+            self.rows = max_rows if max_rows else window + 30 + max_t
+        else:
+            self.rows = max_rows
         self.window, self.ring = window, bool(ring)
         self.handle = B.kvq_alloc(self.cfg, self.k_plane.data_ptr(), self.v_plane.data_ptr(),
                                   self.counters.data_ptr(), self.workspace.data_ptr(),
@@ -119,11 +122,17 @@ class KVCache:
     def set_split_rows(self, rows):
         B.kvq_set_split_rows(self.handle, rows)
 
+    def set_decode_path(self, path, query_bits=0):
+        """path: 0 auto, 1 generic split kernel, 2 warp-specialised kernel."""
+        B.kvq_set_decode_path(self.handle, path, query_bits)
+
     def k_rows(self, seq, phys_lo, phys_hi):
         """Raw K bytes of physical rows [phys_lo, phys_hi) of a sequence (a view)."""
-        v = self.k_plane.view(self.n_seq, self.rows, self.k_tok)
+        n = self.n_seq * self.rows * self.k_tok
+        v = self.k_plane[:n].view(self.n_seq, self.rows, self.k_tok)
         return v[seq, phys_lo:phys_hi]
 
     def v_rows(self, seq, phys_lo, phys_hi):
-        v = self.v_plane.view(self.n_seq, self.rows, self.v_tok)
+        n = self.n_seq * self.rows * self.v_tok
+        v = self.v_plane[:n].view(self.n_seq, self.rows, self.v_tok)
         return v[seq, phys_lo:phys_hi]

@@ -14,6 +14,8 @@
 using namespace kvq;
 
 struct kvq_cache {
+    CUtensorMap kmap;                    // 2-D TMA map of the key plane (warp-specialised decode)
+    bool kmap_ok;
     kvq_config cfg;
     uint8_t* k_plane;
     uint8_t* v_plane;
@@ -26,6 +28,8 @@ struct kvq_cache {
     int max_vis;                         // most rows one decode may read per sequence
     int num_sms;
     int split_rows;                      // 0 = automatic
+    int path;                            // 0 auto, 1 generic split kernel, 2 warp-specialised
+    int nlimb;                           // query limbs of the warp-specialised kernel (2 or 3)
     std::vector<int> len, base;
 };
 
@@ -133,8 +137,9 @@ kvq_status kvq_required_bytes(const kvq_config* cfg, kvq_sizes* out) {
     kvq_status st = check_config(cfg, &g);
     if (st != KVQ_OK) return st;
     if (!out) return fail(KVQ_EINVAL, "out is NULL");
-    out->k_plane = (size_t)cfg->n_seq * g.rows * g.k_tok;
-    out->v_plane = (size_t)cfg->n_seq * g.rows * g.v_tok;
+    // rounded up so that 16-byte aligned tile copies stay inside the planes
+    out->k_plane = round_up((size_t)cfg->n_seq * g.rows * g.k_tok, 256);
+    out->v_plane = round_up((size_t)cfg->n_seq * g.rows * g.v_tok, 256);
     out->counters = counters_bytes(cfg->n_seq);
     out->workspace = ws_layout(cfg, g).total;
     return KVQ_OK;
@@ -176,6 +181,10 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* 
     c->max_vis = g.max_vis;
     c->num_sms = sms;
     c->split_rows = 0;
+    c->kmap_ok = g.k_tok % 16 == 0 &&
+                 make_key_tensor_map(&c->kmap, k_plane, g.k_tok, (long long)cfg->n_seq * g.rows);
+    c->path = 0;
+    c->nlimb = 3;
     c->len.assign(cfg->n_seq, 0);
     c->base.assign(cfg->n_seq, 0);
     e = cudaMemsetAsync(counters, 0, counters_bytes(cfg->n_seq), static_cast<cudaStream_t>(stream));
@@ -290,8 +299,6 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
     const int Hkv = c->cfg.n_kv_heads;
     if (n_q_heads < Hkv || n_q_heads % Hkv || n_q_heads > c->cfg.max_q_heads)
         return fail(KVQ_EINVAL, "n_q_heads must be a multiple of n_kv_heads and <= max_q_heads");
-    if (c->k_tok % 16 || c->v_tok % 16)
-        return fail(KVQ_EUNSUPPORTED, "decode needs n_kv_heads*head_dim to be a multiple of 256");
     const int B = c->cfg.n_seq;
     const int D = c->cfg.head_dim;
     const int hpk = n_q_heads / Hkv;
@@ -299,7 +306,11 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
     const int QC = Q <= 4 ? 4 : 8;
     const int NBH = D / 32;
     const int nK = (QC / 4) * Hkv * NBH;
-    if (2 * nK > kSplitThreads || kSplitThreads % (2 * nK))
+    const bool generic_ok = 2 * nK <= kSplitThreads && kSplitThreads % (2 * nK) == 0;
+    // the warp-specialised kernel needs 16-byte token rows and at most 256 V tasks per row
+    bool fast = c->path != 1 && c->kmap_ok && c->k_tok % 16 == 0 && c->v_tok % 16 == 0 && 2 * nK <= 256 &&
+                Hkv <= 8;
+    if (!fast && !generic_ok)
         return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
     long long total_vis = 0;
     for (int b = 0; b < B; ++b) {
@@ -342,12 +353,38 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
     p.part_o = reinterpret_cast<float*>(c->ws + c->off_part_o);
     p.part_ml = reinterpret_cast<float*>(c->ws + c->off_part_ml);
     p.plan = reinterpret_cast<int*>(c->ws + c->off_plan);
-    p.k_stage_bytes = (uint32_t)round_up((size_t)kTileRows * c->k_tok, 128);
-    p.stage_bytes = p.k_stage_bytes + (uint32_t)round_up((size_t)kTileRows * c->v_tok, 128);
+    // a tile is staged as the 16-byte aligned superset of its rows' bytes
+    p.k_stage_bytes = (uint32_t)round_up((size_t)kTileRows * c->k_tok + 32, 128);
+    p.stage_bytes = p.k_stage_bytes + (uint32_t)round_up((size_t)kTileRows * c->v_tok + 32, 128);
     const int smem_max = split_max_smem();
     p.nstage = 4;
     while (p.nstage > 2 && split_smem_bytes(p) > (size_t)smem_max) --p.nstage;
-    if (split_smem_bytes(p) > (size_t)smem_max)
+    // warp-specialised layout: key rows at an odd multiple of 16 bytes, rings
+    // as deep as shared memory allows, row-group reduction in rounds of heads
+    p.nlimb = c->nlimb;
+    p.k_row_stride = (uint32_t)((c->k_tok / 16 + 1) % 2 ? c->k_tok + 16 : c->k_tok + 32);
+    p.k_boxes = (c->k_tok + 127) / 128;
+    if (fast) {
+        bool fits = false;
+        const int depths[4][2] = {{3, 3}, {3, 2}, {2, 3}, {2, 2}};
+        for (int di = 0; di < 4 && !fits; ++di) {
+            p.nstage_k = depths[di][0];
+            p.nstage_v = depths[di][1];
+            for (p.red_heads = Hkv; p.red_heads >= 1; p.red_heads = p.red_heads > 1 ? (p.red_heads + 1) / 2 : 0) {
+                if (fast_layout(p, p.nlimb).total <= (size_t)smem_max) {
+                    fits = true;
+                    break;
+                }
+                if (p.red_heads == 1) break;
+            }
+        }
+        if (!fits) fast = false;
+    }
+    if (c->path == 2 && !fast)
+        return fail(KVQ_EUNSUPPORTED, "the warp-specialised decode does not support this geometry");
+    if (!fast && !generic_ok)
+        return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
+    if (!fast && split_smem_bytes(p) > (size_t)smem_max)
         return fail(KVQ_EUNSUPPORTED, "decode tile does not fit shared memory (%zu bytes)", split_smem_bytes(p));
     long long items = 0;
     for (int b = 0; b < B; ++b) {
@@ -357,7 +394,7 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
     items *= p.nqs;
     const int grid = (int)std::max(1LL, std::min<long long>(items, c->num_sms));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_split(p, grid, s);
+    cudaError_t e = fast ? launch_split_fast(p, c->kmap, grid, s) : launch_split(p, grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode split kernel");
     MergeParams m;
     m.part_o = p.part_o;
@@ -453,6 +490,16 @@ kvq_status kvq_read_device_error(kvq_cache* c, int* err, void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "read error word");
     e = cudaMemset(c->err_d, 0, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+    return KVQ_OK;
+}
+
+kvq_status kvq_set_decode_path(kvq_cache* c, int path, int query_bits) {
+    if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+    if (path < 0 || path > 2) return fail(KVQ_EINVAL, "path must be 0, 1 or 2");
+    if (query_bits != 0 && query_bits != 16 && query_bits != 24)
+        return fail(KVQ_EINVAL, "query_bits must be 0, 16 or 24");
+    c->path = path;
+    c->nlimb = query_bits == 16 ? 2 : 3;
     return KVQ_OK;
 }
 

@@ -35,125 +35,12 @@
 // At the end of an item the V row groups are summed through shared memory and
 // the partial (max, sum, o[D]) of every query is written out; the merge
 // kernel combines the partials of a sequence with the sink by log-sum-exp.
-#include "kvq_internal.cuh"
-
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
+#include "kvq_device.cuh"
 
 namespace kvq {
 namespace {
 
-constexpr float kNegInf = -__builtin_huge_valf();
-constexpr float kLazy = 8.0f;            // log2 units a score may exceed the reference max
-constexpr int kWaitIters = 1 << 22;      // bounded mbarrier wait
-
-// ------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// bounded wait; false when it ran out
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (int i = 0; i < kWaitIters; ++i)
-        if (mbar_try(bar, parity)) return true;
-    return false;
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ float4 lds128f(uint32_t a) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
-    return v;
-}
-
-__device__ __forceinline__ float load_q(const void* q, long long idx, int bf16) {
-    if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(q)[idx]);
-    return reinterpret_cast<const float*>(q)[idx];
-}
-
-__device__ __forceinline__ float h2f(uint32_t bits16) {
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
-}
-
-// ---------------------------------------------------------- work mapping
-
-struct Item {
-    int b, split, qs, pidx;
-};
-
-// visible-row window of sequence b for a T-row step: rows [lo, len)
-__device__ __forceinline__ void visible_rows(const SplitParams& p, int len, int& lo) {
-    lo = 0;
-    if (p.window > 0) lo = max(0, len - p.T + 1 - p.window);
-}
-
-__device__ __forceinline__ Item item_of(int idx, const int* prefix, int B, int nqs) {
-    Item it;
-    const int pi = idx / nqs;
-    it.qs = idx - pi * nqs;
-    int lo = 0, hi = B;  // largest b with prefix[b] <= pi
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= pi) lo = mid;
-        else hi = mid;
-    }
-    it.b = lo;
-    it.split = pi - prefix[lo];
-    it.pidx = pi;
-    return it;
-}
-
-// rows of the item: [row0, row0 + n), tiles of kTileRows
-struct ItemRows {
-    int row0, n, base, len;
-};
-
-__device__ __forceinline__ ItemRows item_rows(const SplitParams& p, const int* lens, const int* bases,
-                                              const Item& it) {
-    ItemRows r;
-    r.len = lens[it.b];
-    r.base = bases[it.b];
-    int lo;
-    visible_rows(p, r.len, lo);
-    r.row0 = lo + it.split * p.C;
-    r.n = min(p.C, r.len - r.row0);
-    return r;
-}
+using namespace dev;
 
 // ------------------------------------------------------------ the kernel
 
@@ -199,33 +86,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitPara
     }
     if (tid == 0) s_abort = 0;
     __syncthreads();
-    if (tid < 32) {
-        int carry = 0;
-        for (int b0 = 0; b0 < p.B; b0 += 32) {
-            const int b = b0 + tid;
-            int ns = 0;
-            if (b < p.B) {
-                const int len = lens[b];
-                int lo;
-                visible_rows(p, len, lo);
-                const bool bad = len < p.T || len - bases[b] > p.max_rows || lo < bases[b];
-                if (bad) {
-                    if (blockIdx.x == 0) atomicExch(p.err_d, kErrCounter);
-                } else {
-                    ns = (len - lo + p.C - 1) / p.C;
-                }
-            }
-            int x = ns;  // inclusive scan over the warp
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (tid >= o) x += y;
-            }
-            if (b < p.B) prefix[b] = carry + x - ns;
-            carry += __shfl_sync(0xffffffffu, x, 31);
-        }
-        if (tid == 0) prefix[p.B] = carry;
-    }
+    if (tid < 32) plan_splits(p, lens, bases, prefix, tid);
     if (tid == 0) {
         for (int s = 0; s < p.nstage; ++s) mbar_init(smem_u32(&bars[s]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -238,6 +99,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitPara
     if (blockIdx.x == 0)
         for (int b = tid; b <= p.B; b += kSplitThreads) p.plan[b] = prefix[b];
     const int n_items = prefix[p.B] * p.nqs;
+    // let the merge grid launch now; it waits (griddepcontrol.wait) for this
+    // grid to complete before reading any partial
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if ((int)blockIdx.x >= n_items) return;
 
     // ---- producer state (thread 0 only): next tile to issue
@@ -251,12 +115,17 @@ __global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitPara
         const int nr = min(kTileRows, ir.row0 + ir.n - r0);
         const int st = issued % p.nstage;
         const uint32_t bar = smem_u32(&bars[st]);
+        // copy the 16-byte aligned superset of the rows' bytes; the tile then
+        // starts (start mod 16) bytes into the stage
         const long long prow = (long long)it.b * p.max_rows + (r0 - ir.base);
-        const uint32_t kb = (uint32_t)nr * p.k_tok, vb = (uint32_t)nr * p.v_tok;
+        const long long ks = prow * p.k_tok, vs = prow * p.v_tok;
+        const long long ks16 = ks & ~15LL, vs16 = vs & ~15LL;
+        const uint32_t kb = (uint32_t)(((ks + (long long)nr * p.k_tok + 15) & ~15LL) - ks16);
+        const uint32_t vb = (uint32_t)(((vs + (long long)nr * p.v_tok + 15) & ~15LL) - vs16);
         mbar_expect_tx(bar, kb + vb);
         uint8_t* dst = stages + (size_t)st * p.stage_bytes;
-        bulk_g2s(smem_u32(dst), p.k_plane + prow * p.k_tok, kb, bar);
-        bulk_g2s(smem_u32(dst + p.k_stage_bytes), p.v_plane + prow * p.v_tok, vb, bar);
+        bulk_g2s(smem_u32(dst), p.k_plane + ks16, kb, bar);
+        bulk_g2s(smem_u32(dst + p.k_stage_bytes), p.v_plane + vs16, vb, bar);
         ++issued;
         if (++pr_tile * kTileRows >= ir.n) {
             pr_tile = 0;
@@ -325,8 +194,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitPara
         for (int tl = 0; tl < n_tiles; ++tl, ++tile_ctr) {
             const int st = tile_ctr % p.nstage;
             const uint32_t sbase = smem_u32(stages + (size_t)st * p.stage_bytes);
-            const uint32_t ktile = sbase, vtile = sbase + p.k_stage_bytes;
             const int r0 = ir.row0 + tl * kTileRows;
+            const long long prow = (long long)it.b * p.max_rows + (r0 - ir.base);
+            const uint32_t ktile = sbase + (uint32_t)((prow * p.k_tok) & 15);
+            const uint32_t vtile = sbase + p.k_stage_bytes + (uint32_t)((prow * p.v_tok) & 15);
             const int nr = min(kTileRows, ir.row0 + ir.n - r0);
             float* Sb = S + (tile_ctr & 1) * kTileRows * NQ;
 
@@ -597,68 +468,67 @@ __global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitPara
 
 // Merge the partials of one (sequence, query) over its splits, with the sink:
 // M = max(sink, m_s), L = 2^(sink-M) + sum l_s 2^(m_s-M), out = sum o_s 2^(m_s-M) / L
-// (all in log2 units).  CTA = (query record, sequence, 32-dim chunk); warps
-// stride over splits, lanes over dims.
+// (all in log2 units).  CTA = (query record, sequence, 32-dim chunk); each warp
+// folds every 8th split into a running (max, sum, o) with loads issued four
+// splits ahead, then the eight warp states are combined once.
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
-    extern __shared__ float wsh[];                  // [max_splits] weights, then [8][32] partial sums
+    constexpr int NW = kMergeThreads / 32;
     const int gq = blockIdx.x;                      // t * Hq + h
     const int b = blockIdx.y;
-    const int dchunk = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int dim = blockIdx.z * 32 + (threadIdx.x & 31);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int first = p.plan[b];
     const int ns = p.plan[b + 1] - first;
-    const int h = gq % p.Hq;
-    const float LOG2E = 1.4426950408889634f;
-    const float sink = p.sinks ? p.sinks[h] * LOG2E : kNegInf;
-    __shared__ float red[kMergeThreads / 32];
-    __shared__ float s_M, s_L;
-    // max
-    float mx = sink;
-    for (int s = tid; s < ns; s += kMergeThreads)
-        mx = fmaxf(mx, p.part_ml[((long long)(first + s) * p.Qtot + gq) * 2]);
+    const float* ml = p.part_ml + ((long long)first * p.Qtot + gq) * 2;
+    const float* po = p.part_o + ((long long)first * p.Qtot + gq) * p.D + dim;
+    const long long rs = (long long)p.Qtot;        // record stride between splits
+    float M = kNegInf, L = 0.f, acc = 0.f;
+    constexpr int U = 8;                            // splits whose loads are in flight together
+    for (int s0 = warp; s0 < ns; s0 += U * NW) {
+        float m4[U], l4[U], o4[U];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[warp] = mx;
-    __syncthreads();
-    if (tid == 0) {
-        float m = red[0];
-        for (int i = 1; i < kMergeThreads / 32; ++i) m = fmaxf(m, red[i]);
-        s_M = m;
-    }
-    __syncthreads();
-    const float M = s_M;
-    float* w = wsh;
-    float lsum = 0.f;
-    for (int s = tid; s < ns; s += kMergeThreads) {
-        const long long rec = ((long long)(first + s) * p.Qtot + gq) * 2;
-        const float ms = p.part_ml[rec];
-        const float ws = (ms == kNegInf) ? 0.f : exp2f(ms - M);
-        w[s] = ws;
-        lsum += ws * p.part_ml[rec + 1];
-    }
+        for (int u = 0; u < U; ++u) {
+            const int s = s0 + u * NW;
+            const bool ok = s < ns;
+            m4[u] = ok ? ml[s * rs * 2] : kNegInf;
+            l4[u] = ok ? ml[s * rs * 2 + 1] : 0.f;
+            o4[u] = ok ? po[s * rs * p.D] : 0.f;
+        }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-    __syncthreads();
-    if (lane == 0) red[warp] = lsum;
-    __syncthreads();
-    if (tid == 0) {
-        float l = (sink == kNegInf) ? 0.f : exp2f(sink - M);
-        for (int i = 0; i < kMergeThreads / 32; ++i) l += red[i];
-        s_L = l;
+        for (int u = 0; u < U; ++u) {
+            if (m4[u] == kNegInf) continue;
+            const float Mn = fmaxf(M, m4[u]);
+            const float a = (M == kNegInf) ? 0.f : exp2f(M - Mn);
+            const float w = exp2f(m4[u] - Mn);
+            L = L * a + l4[u] * w;
+            acc = acc * a + o4[u] * w;
+            M = Mn;
+        }
     }
-    __syncthreads();
-    const int dim = dchunk * 32 + lane;
-    float acc = 0.f;
-    for (int s = warp; s < ns; s += kMergeThreads / 32)
-        acc += w[s] * p.part_o[((long long)(first + s) * p.Qtot + gq) * p.D + dim];
-    float* part = wsh + ((ns + 31) & ~31);
-    part[warp * 32 + lane] = acc;
+    __shared__ float sM[NW], sL[NW], sA[NW][32];
+    if (lane == 0) {
+        sM[warp] = M;
+        sL[warp] = L;
+    }
+    sA[warp][lane] = acc;
     __syncthreads();
     if (warp == 0) {
-        float tot = 0.f;
-        for (int i = 0; i < kMergeThreads / 32; ++i) tot += part[i * 32 + lane];
-        p.out[(((long long)b * p.Qtot) + gq) * p.D + dim] = tot / s_L;
+        const float LOG2E = 1.4426950408889634f;
+        const float sink = p.sinks ? p.sinks[gq % p.Hq] * LOG2E : kNegInf;
+        float Mt = sink;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) Mt = fmaxf(Mt, sM[w]);
+        float Lt = (sink == kNegInf) ? 0.f : exp2f(sink - Mt);
+        float At = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            if (sM[w] == kNegInf) continue;
+            const float f = exp2f(sM[w] - Mt);
+            Lt += sL[w] * f;
+            At += sA[w][lane] * f;
+        }
+        p.out[(((long long)b * p.Qtot) + gq) * p.D + dim] = At / Lt;
     }
 }
 
@@ -707,12 +577,12 @@ cudaError_t launch_split(const SplitParams& p, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_merge(const MergeParams& p, int T, int max_splits, bool pdl, cudaStream_t s) {
-    const size_t smem = sizeof(float) * ((size_t)((max_splits + 31) & ~31) + kMergeThreads);
-    cudaError_t e = cudaSuccess;
-    if (smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    (void)max_splits;
+    const size_t smem = 0;
+    // same shared-memory carveout as the split kernels, so merge CTAs launched
+    // early (programmatic dependent launch) can wait beside the split CTAs
+    cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.Hq * T), (unsigned)p.B, (unsigned)(p.D / 32));
     cfg.blockDim = dim3(kMergeThreads);

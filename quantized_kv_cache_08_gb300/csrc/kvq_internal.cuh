@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace kvq {
@@ -15,7 +16,9 @@ constexpr int kMaxIdsPerLaunch = 256;
 constexpr int kSplitThreads = 256; // decode split CTA size
 constexpr int kTileRows = 16;      // KV rows staged per pipeline stage
 constexpr int kMinSplitRows = 64;  // smallest rows-per-split the workspace allows
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 1024;
+constexpr int kFastThreads = 512;  // warp-specialised decode CTA size
+constexpr int kFastRows = 32;      // rows per tile of the warp-specialised decode
 
 // device error word codes
 constexpr int kErrCounter = 1;     // a length/base counter was out of range
@@ -61,7 +64,59 @@ struct SplitParams {
     int nstage;
     uint32_t k_stage_bytes;        // kTileRows * k_tok rounded to 128
     uint32_t stage_bytes;          // k + v stage bytes
+    // warp-specialised kernel only
+    int nstage_k, nstage_v;        // depths of the K and V stage rings
+    uint32_t k_row_stride;         // (generic layout only) stride of a staged key row
+    int k_boxes;                   // 128-byte wide TMA boxes per key row
+    int red_heads;                 // KV heads per round of the row-group reduction
+    int nlimb;                     // int8 limbs per quantised query element (2 or 3)
 };
+
+// Shared-memory layout of the warp-specialised decode kernel (host and device).
+struct FastLayout {
+    size_t kstage, vstage, kring, vring, qlimb, qscale, S, P, alpha, mrun, lrun, red, lens, bars, total;
+};
+
+__host__ __device__ inline size_t fl_round(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline FastLayout fast_layout(const SplitParams& p, int nlimb) {
+    FastLayout L;
+    const size_t NQ = (size_t)p.Hkv * p.QC;
+    const size_t NBH = (size_t)p.D / 32;
+    const size_t nV = 2 * (size_t)(p.QC / 4) * p.Hkv * NBH;
+    const size_t rpV = nV ? 256 / nV : 1;
+    // key tiles: k_boxes swizzled boxes of kFastRows x 128 bytes (1024-byte aligned)
+    L.kstage = (size_t)p.k_boxes * kFastRows * 128;
+    L.vstage = fl_round((size_t)kFastRows * p.v_tok, 128);
+    size_t off = 0;
+    L.kring = off;
+    off += (size_t)p.nstage_k * L.kstage;
+    L.vring = off;
+    off += (size_t)p.nstage_v * L.vstage;
+    L.qlimb = off;
+    off += fl_round(NQ * p.D * nlimb, 16);
+    L.qscale = off;
+    off += fl_round(NQ * NBH * 4, 16);
+    L.S = off;
+    off += fl_round(2 * NQ * kFastRows * 4, 16);
+    L.P = off;
+    off += fl_round(2 * (size_t)kFastRows * (NQ + 4) * 4, 16);
+    L.alpha = off;
+    off += fl_round(2 * NQ * 4, 16);
+    L.mrun = off;
+    off += fl_round(NQ * 4, 16);
+    L.lrun = off;
+    off += fl_round(NQ * 4, 16);
+    L.red = off;
+    const size_t red_floats = (rpV > 1 ? rpV - 1 : 1) * (size_t)p.red_heads * p.QC * p.D;
+    off += fl_round(red_floats * 4, 16);
+    L.lens = off;
+    off += fl_round((3 * (size_t)p.B + 1) * 4, 16);
+    L.bars = off;
+    off += 8 * (size_t)(p.nstage_k + p.nstage_v);
+    L.total = off + 1024;          // slack to align the base to 1024 bytes
+    return L;
+}
 
 struct MergeParams {
     const float* part_o;
@@ -84,6 +139,10 @@ cudaError_t launch_set_base(int* base_d, int seq, int value, cudaStream_t s);
 size_t split_smem_bytes(const SplitParams& p);
 int split_max_smem();
 cudaError_t launch_split(const SplitParams& p, int grid, cudaStream_t s);
+// warp-specialised decode (kvq_decode_fast.cu): token rows must be 16-byte multiples
+cudaError_t launch_split_fast(const SplitParams& p, const CUtensorMap& kmap, int grid, cudaStream_t s);
+// 2-D TMA map of a key plane: rows x k_tok bytes, boxes of kFastRows x 128 bytes, 128-byte swizzle
+bool make_key_tensor_map(CUtensorMap* map, void* k_plane, int k_tok, long long rows);
 cudaError_t launch_merge(const MergeParams& p, int T, int max_splits, bool pdl, cudaStream_t s);
 
 }  // namespace kvq

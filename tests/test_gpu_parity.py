@@ -120,13 +120,22 @@ CASES = [
     (2, 16, 8, 32, [130, 64], 3, 0, False, True, torch.float32),
     (1, 32, 8, 64, [257], 2, 0, False, False, torch.float32),
     (4, 8, 2, 128, [5, 17, 64, 65], 4, 0, False, True, torch.float32),
+    # token rows that are not 16-byte multiples (generic kernel only)
+    (2, 4, 1, 128, [300, 45], 1, 0, False, True, torch.float32),
+    (1, 6, 1, 64, [222], 2, 0, False, False, torch.float32),
+    (1, 8, 2, 64, [129], 1, 40, False, False, torch.float32),
 ]
 
+# (kernel path, query bits): 1 = generic split kernel, 2 = warp-specialised
+PATHS = [(1, 0), (2, 24), (2, 16)]
 
+
+@pytest.mark.parametrize("path", PATHS, ids=["generic", "ws24", "ws16"])
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
-def test_decode_matches_oracle(case):
+def test_decode_matches_oracle(case, path):
     Bn, Hq, Hkv, D, lens, T, window, ring, sinks, qdt = case
     p = Pair(Bn, Hkv, D, Hq, max_t=max(T, 64), max_rows=max(lens) + T, window=window, ring=ring)
+    p.dev.set_decode_path(*path)
     for b, L in enumerate(lens):
         k = _randn(1, L, Hkv, D, seed=100 + b)
         v = _randn(1, L, Hkv, D, seed=200 + b)
@@ -134,13 +143,21 @@ def test_decode_matches_oracle(case):
             p.append(k[:, t0:t0 + 64], v[:, t0:t0 + 64], seq_ids=[b])
     q = _randn(Bn, T, Hq, D, seed=7).to(qdt)
     s = _randn(Hq, seed=8) if sinks else None
+    if path[0] == 2 and (Hkv * D) % 256:
+        with pytest.raises(B.KvqError) as e:
+            p.decode(q, sinks=s)
+        assert e.value.status == B.KVQ_EUNSUPPORTED
+        return
     got, ref = p.decode(q, sinks=s)
-    assert_close(got, ref)
+    err = assert_close(got, ref)
+    if path != (2, 16):
+        assert err <= 2e-5, f"fp32-level path error {err:.2e}"
     assert p.dev.device_error() == 0
 
 
+@pytest.mark.parametrize("path", [1, 2])
 @pytest.mark.parametrize("split_rows", [64, 72, 128, 1000, 4096])
-def test_decode_split_sizes_agree(split_rows):
+def test_decode_split_sizes_agree(split_rows, path):
     Hq, Hkv, D, L = 32, 8, 128, 3000
     p = Pair(2, Hkv, D, Hq, max_t=64, max_rows=L)
     for b in range(2):
@@ -148,6 +165,7 @@ def test_decode_split_sizes_agree(split_rows):
         for t0 in range(0, k.shape[1], 64):
             p.append(k[:, t0:t0 + 64], 0.5 * k[:, t0:t0 + 64], seq_ids=[b])
     p.dev.set_split_rows(split_rows)
+    p.dev.set_decode_path(path)
     q = _randn(2, 1, Hq, D, seed=9)
     got, ref = p.decode(q)
     assert_close(got, ref)
@@ -242,12 +260,14 @@ def test_truncate_then_reappend_equals_clean_build():
     assert e.value.status == B.KVQ_ERANGE
 
 
-def test_ring_growth_matches_flat_oracle_and_keeps_invariants():
+@pytest.mark.parametrize("path", [1, 2])
+def test_ring_growth_matches_flat_oracle_and_keeps_invariants(path):
     """A small ring (window 64 + 31 rows) grown to 600 rows, T=1 steps: the
     live rows equal the oracle's logical rows, at most 31 masked rows precede
     the window, and outputs match the windowed oracle at every step."""
-    Hq, Hkv, D, W, N = 16, 2, 64, 64, 600
+    Hq, Hkv, D, W, N = 16, 4, 64, 64, 600
     p = Pair(1, Hkv, D, Hq, max_t=1, window=W, ring=True)
+    p.dev.set_decode_path(path)
     assert p.dev.rows == W + 31
     k = _randn(1, N, Hkv, D, seed=91)
     v = _randn(1, N, Hkv, D, seed=92)
