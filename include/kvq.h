@@ -91,9 +91,10 @@ typedef struct kvq_config {
 } kvq_config;
 
 /* Device bytes the caller provides (each buffer 16-byte aligned):
- *   k_plane   [n_seq][max_rows][kb*34]  kb = n_kv_heads*head_dim/32, size
- *             rounded up to a multiple of 256 bytes
- *   v_plane   [n_seq][max_rows][kb*24]  (likewise rounded up)
+ *   k_plane   [n_seq][max_rows][kb*34]  kb = n_kv_heads*head_dim/32, plus
+ *             128 bytes of padding (tile copies move whole 128-byte column
+ *             blocks), rounded up to a multiple of 256 bytes
+ *   v_plane   [n_seq][max_rows][kb*24]  (padded and rounded likewise)
  *   counters  len_d[n_seq], base_d[n_seq], error word (int32)
  *   workspace decode partials, the split plan and the ring-rebase scratch   */
 typedef struct kvq_sizes {

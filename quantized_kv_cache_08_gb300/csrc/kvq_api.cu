@@ -14,7 +14,7 @@
 using namespace kvq;
 
 struct kvq_cache {
-    CUtensorMap kmap;                    // 2-D TMA map of the key plane (warp-specialised decode)
+    CUtensorMap kmap, vmap;              // 3-D TMA maps of the planes (warp-specialised decode)
     bool kmap_ok;
     kvq_config cfg;
     uint8_t* k_plane;
@@ -137,9 +137,10 @@ kvq_status kvq_required_bytes(const kvq_config* cfg, kvq_sizes* out) {
     kvq_status st = check_config(cfg, &g);
     if (st != KVQ_OK) return st;
     if (!out) return fail(KVQ_EINVAL, "out is NULL");
-    // rounded up so that 16-byte aligned tile copies stay inside the planes
-    out->k_plane = round_up((size_t)cfg->n_seq * g.rows * g.k_tok, 256);
-    out->v_plane = round_up((size_t)cfg->n_seq * g.rows * g.v_tok, 256);
+    // rounded up and padded by 128 bytes: tile copies read whole 16-byte
+    // chunks and whole 128-byte column blocks, which may pass the last row
+    out->k_plane = round_up((size_t)cfg->n_seq * g.rows * g.k_tok + 128, 256);
+    out->v_plane = round_up((size_t)cfg->n_seq * g.rows * g.v_tok + 128, 256);
     out->counters = counters_bytes(cfg->n_seq);
     out->workspace = ws_layout(cfg, g).total;
     return KVQ_OK;
@@ -181,8 +182,9 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* 
     c->max_vis = g.max_vis;
     c->num_sms = sms;
     c->split_rows = 0;
-    c->kmap_ok = g.k_tok % 16 == 0 &&
-                 make_key_tensor_map(&c->kmap, k_plane, g.k_tok, (long long)cfg->n_seq * g.rows);
+    c->kmap_ok = g.k_tok % 16 == 0 && g.v_tok % 16 == 0 &&
+                 make_row_tensor_map(&c->kmap, k_plane, g.k_tok, (long long)cfg->n_seq * g.rows) &&
+                 make_row_tensor_map(&c->vmap, v_plane, g.v_tok, (long long)cfg->n_seq * g.rows);
     c->path = 0;
     c->nlimb = 3;
     c->len.assign(cfg->n_seq, 0);
@@ -308,8 +310,7 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
     const int nK = (QC / 4) * Hkv * NBH;
     const bool generic_ok = 2 * nK <= kSplitThreads && kSplitThreads % (2 * nK) == 0;
     // the warp-specialised kernel needs 16-byte token rows and at most 256 V tasks per row
-    bool fast = c->path != 1 && c->kmap_ok && c->k_tok % 16 == 0 && c->v_tok % 16 == 0 && 2 * nK <= 256 &&
-                Hkv <= 8;
+    bool fast = c->path != 1 && c->kmap_ok && 2 * nK <= 256 && (2 * nK) % 8 == 0 && Hkv <= 8;
     if (!fast && !generic_ok)
         return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
     long long total_vis = 0;
@@ -364,19 +365,15 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
     p.nlimb = c->nlimb;
     p.k_row_stride = (uint32_t)((c->k_tok / 16 + 1) % 2 ? c->k_tok + 16 : c->k_tok + 32);
     p.k_boxes = (c->k_tok + 127) / 128;
+    p.v_boxes = (c->v_tok + 127) / 128;
     if (fast) {
         bool fits = false;
         const int depths[4][2] = {{3, 3}, {3, 2}, {2, 3}, {2, 2}};
+        p.red_heads = 1;
         for (int di = 0; di < 4 && !fits; ++di) {
             p.nstage_k = depths[di][0];
             p.nstage_v = depths[di][1];
-            for (p.red_heads = Hkv; p.red_heads >= 1; p.red_heads = p.red_heads > 1 ? (p.red_heads + 1) / 2 : 0) {
-                if (fast_layout(p, p.nlimb).total <= (size_t)smem_max) {
-                    fits = true;
-                    break;
-                }
-                if (p.red_heads == 1) break;
-            }
+            fits = fast_layout(p, p.nlimb).total <= (size_t)smem_max;
         }
         if (!fits) fast = false;
     }
@@ -394,7 +391,7 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
     items *= p.nqs;
     const int grid = (int)std::max(1LL, std::min<long long>(items, c->num_sms));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = fast ? launch_split_fast(p, c->kmap, grid, s) : launch_split(p, grid, s);
+    cudaError_t e = fast ? launch_split_fast(p, c->kmap, c->vmap, grid, s) : launch_split(p, grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode split kernel");
     MergeParams m;
     m.part_o = p.part_o;

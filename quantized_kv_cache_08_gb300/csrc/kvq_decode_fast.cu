@@ -28,9 +28,11 @@
 // reference maximum moves only when a score exceeds it by more than 8 (log2
 // units); a warp vote finds that rare case, otherwise p = 2^(s - m_ref) needs
 // no reduction and each lane keeps a partial sum of p until the item ends.
-// V warps, accumulation: one thread per (query group of 4, KV head, block,
-// half block); the 5-bit codes are rebuilt with byte arithmetic and placed in
-// the mantissa of 0.5 (value 0.5 + u/256), so v_hat = 256 d F + (m - 128 d)
+// V warps, accumulation: a task is (query group of 4, KV head, block, half
+// block); a warp holds TW consecutive tasks and 32/TW lane groups that take
+// interleaved rows, so the row partial sums reduce with warp shuffles at the
+// end of an item.  The 5-bit codes are rebuilt with byte arithmetic and placed
+// in the mantissa of 0.5 (value 0.5 + u/256), so v_hat = 256 d F + (m - 128 d)
 // and o += (256 p d) F with packed FMAs, plus sum p (m - 128 d) per block.
 #include "kvq_device.cuh"
 
@@ -41,8 +43,9 @@ using namespace dev;
 
 constexpr int kThreads = kFastThreads;
 constexpr int kRows = kFastRows;
+constexpr int kSDepth = kFastSDepth;               // score buffers between K and V warps
 constexpr int kKThreads = 256;                 // warps 0-7
-constexpr int BAR_K = 1, BAR_FULL = 2, BAR_EMPTY = 4, BAR_V = 6, BAR_QLOAD = 7;
+constexpr int BAR_K = 1, BAR_V = 2, BAR_QLOAD = 3, BAR_FULL = 4, BAR_EMPTY = 4 + kSDepth;
 constexpr long long kWaitCycles = 1LL << 31;   // ~1 s bound on any mbarrier wait
 
 __device__ __forceinline__ void bar_sync(int id, int n) {
@@ -56,12 +59,20 @@ __device__ __forceinline__ uint4 lds128u(uint32_t a) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
     return v;
 }
-// 2-D TMA tile load of box {x, y} of a tensor map into shared memory
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// 3-D TMA tile load of box {0, y, 0} of a tensor map into shared memory
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* map, int y, uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(0), "r"(bar)
         : "memory");
+}
+
+// Byte `col` of staged row `r` in a tile laid out by tma_load_rows: column
+// block col / 128 holds the 32 rows at 128 bytes each, 16-byte chunk j of
+// row r stored at chunk j ^ (r & 7) (the TMA 128-byte swizzle).
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int r, int col) {
+    return base + (uint32_t)(col >> 7) * (kFastRows * 128) + (uint32_t)r * 128u +
+           ((((uint32_t)col >> 4) & 7u) ^ ((uint32_t)r & 7u)) * 16u + ((uint32_t)col & 15u);
 }
 __device__ __forceinline__ int dp4a_su(unsigned a, unsigned b, int c) {   // a: 4 x s8, b: 4 x u8
     int d;
@@ -267,17 +278,9 @@ __device__ __forceinline__ void head_scores_dispatch(uint32_t kbase, uint32_t ro
     }
 }
 
-// Float4 slot of (query row qr, dim) in a [rows][D] reduction slice, with the
-// low bits of the slot index XOR-ed by the block and head bits so that the
-// threads of a warp (different blocks, halves and heads) hit different banks.
-template <int D>
-__device__ __forceinline__ int red_slot(int qr, int dim) {
-    const int f4 = (qr * D + dim) >> 2;
-    return f4 ^ (((f4 >> 3) & 3) << 1) ^ ((f4 >> (D / 4 == 8 ? 3 : 5)) & 1);
-}
-
 template <int NBH, int NQG, int NLIMB>
-__global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, const __grid_constant__ CUtensorMap kmap) {
+__global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, const __grid_constant__ CUtensorMap kmap,
+                                                            const __grid_constant__ CUtensorMap vmap) {
     constexpr int QC = 4 * NQG;
     constexpr int D = NBH * 32;
     constexpr int NQMAX = 32 * NQG;                 // CTA queries (Hkv * QC, Hkv <= 8): <= 4 * NQG per softmax warp
@@ -295,10 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
     uint8_t* vring = smem + L.vring;
     uint32_t* qlimb = reinterpret_cast<uint32_t*>(smem + L.qlimb);
     float* qscl = reinterpret_cast<float*>(smem + L.qscale);
-    float* S = reinterpret_cast<float*>(smem + L.S);            // [2][NQ][kRows]
+    float* S = reinterpret_cast<float*>(smem + L.S);            // [kSDepth][NQ][kRows]
     float* P = reinterpret_cast<float*>(smem + L.P);            // [2][kRows][PS]
     float* alpha = reinterpret_cast<float*>(smem + L.alpha);    // [2][NQ]
-    float* red = reinterpret_cast<float*>(smem + L.red);
     int* qlo = reinterpret_cast<int*>(smem + L.mrun);           // [NQ] first visible row per CTA query
     int* qup = reinterpret_cast<int*>(smem + L.lrun);           // [NQ] one past the last (-1: no query)
     int* lens = reinterpret_cast<int*>(smem + L.lens);
@@ -431,8 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
             wait_stage(smem_u32(&kbar[kst]), (uint32_t)((jt / p.nstage_k) & 1), &s_abort, p.err_d);
             const uint32_t kbase = smem_u32(kring + (size_t)kst * L.kstage);
             const uint32_t rowoff = (uint32_t)lane * 128u, sw = (uint32_t)lane & 7u;
-            if (jt >= 2) bar_sync(BAR_EMPTY + (jt & 1), kThreads);  // V done with buffers of tile jt-2
-            float* Sb = S + (jt & 1) * NQ * kRows;
+            const int sb = jt % kSDepth;
+            if (jt >= kSDepth) bar_sync(BAR_EMPTY + sb, kThreads);  // V has read the scores of tile jt-kSDepth
+            float* Sb = S + sb * NQ * kRows;
             const int row = ti.r0 + lane;
 #pragma unroll 1
             for (int unit = warp; unit < Hkv * NQG; unit += 8) {
@@ -450,30 +453,27 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                     Sb[(qq0 + n) * kRows + lane] = vis ? sc[n] : kNegInf;
                 }
             }
-            bar_arrive(BAR_FULL + (jt & 1), kThreads);     // scores of tile jt; K stage jt is free
+            bar_arrive(BAR_FULL + sb, kThreads);           // scores of tile jt; K stage jt is free
             advance(c, ti, p, lens, bases, prefix, n_items);
             ++jt;
         }
-        for (int j = max(2, jt); j < jt + 2; ++j) bar_sync(BAR_EMPTY + (j & 1), kThreads);
+        for (int j = max(kSDepth, jt); j < jt + kSDepth; ++j) bar_sync(BAR_EMPTY + j % kSDepth, kThreads);
     } else {
         // ======================================================== V warps
-        // copy issue (K and V tiles), online softmax, p * v_hat accumulation
+        // copy issue, online softmax, p * v_hat accumulation
         const int vt = tid - kKThreads;
         const int vw = warp - 8;
-        // key tile: k_boxes swizzled 32-row x 128-byte TMA boxes (out-of-range
-        // rows and columns are filled with zeros and never scored); value tile:
-        // one bulk copy.  Only V thread 0 issues; its cursors live in shared memory.
+        // key and value tiles: one 3-D TMA box each (32 rows x all column
+        // blocks, 128-byte swizzle).  V thread 0 issues; its cursors live in
+        // shared memory.
         auto issue_k = [&]() {
             Cursor kc = s_kc;
             if (kc.item >= n_items) return;
             const TileInfo ti = tile_of(kc);
             const int st = s_k_issued % p.nstage_k;
             const uint32_t bar = smem_u32(&kbar[st]);
-            const int grow = ti.b * p.max_rows + (ti.r0 - ti.base);
             mbar_expect_tx(bar, (uint32_t)L.kstage);
-            const uint32_t dst = smem_u32(kring + (size_t)st * L.kstage);
-            for (int bx = 0; bx < p.k_boxes; ++bx)
-                tma_load_2d(dst + (uint32_t)bx * (kFastRows * 128), &kmap, bx * 128, grow, bar);
+            tma_load_rows(smem_u32(kring + (size_t)st * L.kstage), &kmap, ti.b * p.max_rows + (ti.r0 - ti.base), bar);
             ++s_k_issued;
             advance(kc, ti, p, lens, bases, prefix, n_items);
             s_kc = kc;
@@ -484,10 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
             const TileInfo ti = tile_of(vc);
             const int st = s_v_issued % p.nstage_v;
             const uint32_t bar = smem_u32(&vbar[st]);
-            const long long prow = (long long)ti.b * p.max_rows + (ti.r0 - ti.base);
-            const uint32_t bytes = (uint32_t)ti.nr * p.v_tok;
-            mbar_expect_tx(bar, bytes);
-            bulk_g2s(smem_u32(vring + (size_t)st * L.vstage), p.v_plane + prow * p.v_tok, bytes, bar);
+            mbar_expect_tx(bar, (uint32_t)L.vstage);
+            tma_load_rows(smem_u32(vring + (size_t)st * L.vstage), &vmap, ti.b * p.max_rows + (ti.r0 - ti.base), bar);
             ++s_v_issued;
             advance(vc, ti, p, lens, bases, prefix, n_items);
             s_vc = vc;
@@ -510,15 +508,20 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
             m_ref[i] = kNegInf;
             lsum[i] = 0.f;
         }
-        // accumulation task
-        const int nV = 2 * NQG * Hkv * NBH;
-        const int rpV = kKThreads / nV;
-        const bool v_active = vt < rpV * nV;
-        const int v_rg = vt / nV, v_task = vt % nV;
+        // accumulation task: TW tasks per warp (consecutive lanes), the warp's
+        // 32 / TW lane groups take interleaved rows of the tile, so partial
+        // sums over rows meet inside the warp and reduce with shuffles
+        const int nV = 2 * NQG * Hkv * NBH;             // tasks per row
+        const int TW = nV / 8;                          // tasks per warp
+        const int RG = 32 / TW;                         // row groups (lane groups) per warp
+        // lanes past TW * RG (TW not a power of two) hold no rows
+        const int v_task = vw * TW + lane % TW, v_rg = lane / TW;
         const int v_hf = v_task & 1, v_bi = (v_task >> 1) % NBH, v_g = (v_task >> 1) / NBH % Hkv;
         const int v_qg = (v_task >> 1) / (NBH * Hkv);
         const int v_blk = v_g * NBH + v_bi;
         const int v_qq0 = v_g * QC + 4 * v_qg;
+        const int col_dm = v_blk * kQ5Bytes;            // d, m, qh of the thread's block
+        const int col_qs = col_dm + 8 + 8 * v_hf;       // its 8 bytes of qs
         float2 o2[4][8];
         float pm[4];
 #pragma unroll
@@ -531,13 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
         int jt = 0;
         while (c.item < n_items) {
             const TileInfo ti = tile_of(c);
-            bar_sync(BAR_FULL + (jt & 1), kThreads);     // scores of tile jt are in
-            if (vt == 0) {
-                issue_k();                                 // K stage of tile jt is free
-                if (jt >= 1) issue_v();                    // V stage of tile jt-1 is free
-            }
+            const int sb = jt % kSDepth;
+            bar_sync(BAR_FULL + sb, kThreads);             // scores of tile jt are in
             // ------------------------------------------------ online softmax
-            const float* Sb = S + (jt & 1) * NQ * kRows;
+            const float* Sb = S + sb * NQ * kRows;
             float* Pb = P + (jt & 1) * kRows * PS;
             float* ab = alpha + (jt & 1) * NQ;
 #pragma unroll
@@ -561,12 +561,17 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                     if (lane == 0) ab[qq] = al;
                 }
             }
-            bar_sync(BAR_V, kKThreads);                    // p and alpha of tile jt written
+            bar_arrive(BAR_EMPTY + sb, kThreads);          // scores of tile jt consumed
+            bar_sync(BAR_V, kKThreads);                    // p and alpha of tile jt written; V stage jt-1 free
+            if (vt == 0) {
+                issue_k();                                 // K stage of tile jt is free (FULL passed)
+                if (jt >= 1) issue_v();                    // V stage of tile jt-1 is free (BAR_V passed)
+            }
             // ------------------------------------------------ accumulate
             const int vst = jt % p.nstage_v;
             wait_stage(smem_u32(&vbar[vst]), (uint32_t)((jt / p.nstage_v) & 1), &s_abort, p.err_d);
             const uint32_t vtile = smem_u32(vring + (size_t)vst * L.vstage);
-            if (v_active) {
+            {
                 const float4 al4 = *reinterpret_cast<const float4*>(&ab[v_qq0]);
                 const float alv[4] = {al4.x, al4.y, al4.z, al4.w};
 #pragma unroll
@@ -581,10 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                     }
                 }
                 const uint32_t pb = smem_u32(Pb);
-                for (int r = v_rg; r < ti.nr; r += rpV) {
-                    const uint32_t vb = vtile + (uint32_t)(r * p.v_tok + v_blk * kQ5Bytes);
-                    const uint2 dmqh = lds64(vb);
-                    const uint2 qs = lds64(vb + 8 + 8 * v_hf);
+                for (int r = v_rg < RG ? v_rg : kRows; r < ti.nr; r += RG) {
+                    const uint2 dmqh = lds64(tile_addr(vtile, r, col_dm));
+                    const uint2 qs = lds64(tile_addr(vtile, r, col_qs));
                     const float4 p4 = lds128f(pb + 4u * (uint32_t)(r * PS + v_qq0));
                     const float d = h2f(dmqh.x & 0xffffu);
                     const float m = h2f(dmqh.x >> 16);
@@ -625,68 +629,28 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                     }
                 }
             }
-            bar_arrive(BAR_EMPTY + (jt & 1), kThreads);    // buffers and V stage of tile jt done
             if (ti.last) {
-                // Sum the accumulation row groups through shared memory, a few
-                // heads per round; row group 0 keeps the totals in registers.
-                // Global stores come only after the last barrier: a barrier
-                // waits for its threads' outstanding global stores.
-                for (int g0 = 0; g0 < Hkv; g0 += p.red_heads) {
-                    const bool mine = v_active && v_g >= g0 && v_g < g0 + p.red_heads;
-                    float4* red4 = reinterpret_cast<float4*>(red);
-                    const int slice = p.red_heads * QC * D / 4;            // float4 slots per row group
-                    if (mine && v_rg > 0) {
-                        float4* dst = red4 + (size_t)(v_rg - 1) * slice;
+                // row-group partial sums meet inside the warp: tree-reduce
+                // down the lane groups, lane group 0 ends with the sum
+                for (int st = 1; st < RG; st <<= 1) {
+                    const bool take = v_rg + st < RG;
+                    const int dl = st * TW;
 #pragma unroll
-                        for (int n = 0; n < 4; ++n) {
-                            const int qr = (v_g - g0) * QC + 4 * v_qg + n;
+                    for (int n = 0; n < 4; ++n) {
+                        const float a = __shfl_down_sync(0xffffffffu, pm[n], dl);
+                        if (take) pm[n] += a;
 #pragma unroll
-                            for (int cc = 0; cc < 4; ++cc) {
-                                const int dim = v_bi * 32 + 8 * v_hf + (cc & 1) * 4 + (cc >> 1) * 16;
-                                dst[red_slot<D>(qr, dim)] =
-                                    make_float4(o2[n][2 * cc].x + pm[n], o2[n][2 * cc].y + pm[n],
-                                                o2[n][2 * cc + 1].x + pm[n], o2[n][2 * cc + 1].y + pm[n]);
+                        for (int i = 0; i < 8; ++i) {
+                            const float x = __shfl_down_sync(0xffffffffu, o2[n][i].x, dl);
+                            const float y = __shfl_down_sync(0xffffffffu, o2[n][i].y, dl);
+                            if (take) {
+                                o2[n][i].x += x;
+                                o2[n][i].y += y;
                             }
                         }
                     }
-                    bar_sync(BAR_V, kKThreads);
-                    if (mine && v_rg == 0) {
-#pragma unroll
-                        for (int n = 0; n < 4; ++n) {
-#pragma unroll
-                            for (int cc = 0; cc < 4; ++cc) {
-                                o2[n][2 * cc].x += pm[n];
-                                o2[n][2 * cc].y += pm[n];
-                                o2[n][2 * cc + 1].x += pm[n];
-                                o2[n][2 * cc + 1].y += pm[n];
-                            }
-                            pm[n] = 0.f;
-                        }
-                        // one row group at a time, its 16 loads independent of each other
-                        for (int g2 = 0; g2 < rpV - 1; ++g2) {
-                            const float4* srcg = red4 + (size_t)g2 * slice;
-                            float4 o[4][4];
-#pragma unroll
-                            for (int n = 0; n < 4; ++n) {
-                                const int qr = (v_g - g0) * QC + 4 * v_qg + n;
-#pragma unroll
-                                for (int cc = 0; cc < 4; ++cc)
-                                    o[n][cc] = srcg[red_slot<D>(qr, v_bi * 32 + 8 * v_hf + (cc & 1) * 4 + (cc >> 1) * 16)];
-                            }
-#pragma unroll
-                            for (int n = 0; n < 4; ++n)
-#pragma unroll
-                                for (int cc = 0; cc < 4; ++cc) {
-                                    o2[n][2 * cc].x += o[n][cc].x;
-                                    o2[n][2 * cc].y += o[n][cc].y;
-                                    o2[n][2 * cc + 1].x += o[n][cc].z;
-                                    o2[n][2 * cc + 1].y += o[n][cc].w;
-                                }
-                        }
-                    }
-                    bar_sync(BAR_V, kKThreads);
                 }
-                if (v_active && v_rg == 0) {
+                if (v_rg == 0) {
 #pragma unroll
                     for (int n = 0; n < 4; ++n) {
                         const int qi = ti.it.qs * QC + 4 * v_qg + n;
@@ -697,8 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                             for (int cc = 0; cc < 4; ++cc) {
                                 const int dim = v_bi * 32 + 8 * v_hf + (cc & 1) * 4 + (cc >> 1) * 16;
                                 *reinterpret_cast<float4*>(&p.part_o[rec * D + dim]) =
-                                    make_float4(o2[n][2 * cc].x, o2[n][2 * cc].y, o2[n][2 * cc + 1].x,
-                                                o2[n][2 * cc + 1].y);
+                                    make_float4(o2[n][2 * cc].x + pm[n], o2[n][2 * cc].y + pm[n],
+                                                o2[n][2 * cc + 1].x + pm[n], o2[n][2 * cc + 1].y + pm[n]);
                             }
                         }
                     }
@@ -737,17 +701,18 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
 }
 
 template <int NBH, int NQG, int NLIMB>
-cudaError_t launch_t(const SplitParams& p, const CUtensorMap& kmap, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_t(const SplitParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid, size_t smem,
+                     cudaStream_t s) {
     auto fn = fast_kernel<NBH, NQG, NLIMB>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    fn<<<grid, kThreads, smem, s>>>(p, kmap);
+    fn<<<grid, kThreads, smem, s>>>(p, kmap, vmap);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-bool make_key_tensor_map(CUtensorMap* map, void* k_plane, int k_tok, long long rows) {
+bool make_row_tensor_map(CUtensorMap* map, void* plane, int tok_bytes, long long rows) {
     using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -761,20 +726,26 @@ bool make_key_tensor_map(CUtensorMap* map, void* k_plane, int k_tok, long long r
             return false;
         encode = reinterpret_cast<Encode>(fn);
     }
-    const cuuint64_t dims[2] = {(cuuint64_t)k_tok, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)k_tok};
-    const cuuint32_t box[2] = {128, (cuuint32_t)kFastRows};
-    const cuuint32_t estr[2] = {1, 1};
-    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k_plane, dims, strides, box, estr,
+    // dims: byte within a 128-byte column block, row, column block; the last
+    // block of a row may reach up to 127 bytes into the next row (or into the
+    // plane padding kvq_required_bytes adds)
+    const int blocks = (tok_bytes + 127) / 128;
+    if (blocks > 256) return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)blocks};
+    const cuuint64_t strides[2] = {(cuuint64_t)tok_bytes, 128};
+    const cuuint32_t box[3] = {128, (cuuint32_t)kFastRows, (cuuint32_t)blocks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, plane, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_split_fast(const SplitParams& p, const CUtensorMap& kmap, int grid, cudaStream_t s) {
+cudaError_t launch_split_fast(const SplitParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
+                              cudaStream_t s) {
     const size_t smem = fast_layout(p, p.nlimb).total;
     const int NBH = p.D / 32, NQG = p.QC / 4;
 #define KVQ_CASE(nb, nq, nl) \
-    if (NBH == nb && NQG == nq && p.nlimb == nl) return launch_t<nb, nq, nl>(p, kmap, grid, smem, s);
+    if (NBH == nb && NQG == nq && p.nlimb == nl) return launch_t<nb, nq, nl>(p, kmap, vmap, grid, smem, s);
     KVQ_CASE(1, 1, 3) KVQ_CASE(2, 1, 3) KVQ_CASE(4, 1, 3) KVQ_CASE(8, 1, 3) KVQ_CASE(16, 1, 3)
     KVQ_CASE(1, 2, 3) KVQ_CASE(2, 2, 3) KVQ_CASE(4, 2, 3) KVQ_CASE(8, 2, 3) KVQ_CASE(16, 2, 3)
     KVQ_CASE(1, 1, 2) KVQ_CASE(2, 1, 2) KVQ_CASE(4, 1, 2) KVQ_CASE(8, 1, 2) KVQ_CASE(16, 1, 2)

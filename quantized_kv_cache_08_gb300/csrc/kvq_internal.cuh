@@ -19,6 +19,7 @@ constexpr int kMinSplitRows = 64;  // smallest rows-per-split the workspace allo
 constexpr int kMergeThreads = 1024;
 constexpr int kFastThreads = 512;  // warp-specialised decode CTA size
 constexpr int kFastRows = 32;      // rows per tile of the warp-specialised decode
+constexpr int kFastSDepth = 4;     // score buffers between its key and value warps
 
 // device error word codes
 constexpr int kErrCounter = 1;     // a length/base counter was out of range
@@ -67,7 +68,8 @@ struct SplitParams {
     // warp-specialised kernel only
     int nstage_k, nstage_v;        // depths of the K and V stage rings
     uint32_t k_row_stride;         // (generic layout only) stride of a staged key row
-    int k_boxes;                   // 128-byte wide TMA boxes per key row
+    int k_boxes;                   // 128-byte column blocks per key row
+    int v_boxes;                   // 128-byte column blocks per value row
     int red_heads;                 // KV heads per round of the row-group reduction
     int nlimb;                     // int8 limbs per quantised query element (2 or 3)
 };
@@ -87,7 +89,7 @@ __host__ __device__ inline FastLayout fast_layout(const SplitParams& p, int nlim
     const size_t rpV = nV ? 256 / nV : 1;
     // key tiles: k_boxes swizzled boxes of kFastRows x 128 bytes (1024-byte aligned)
     L.kstage = (size_t)p.k_boxes * kFastRows * 128;
-    L.vstage = fl_round((size_t)kFastRows * p.v_tok, 128);
+    L.vstage = (size_t)p.v_boxes * kFastRows * 128;
     size_t off = 0;
     L.kring = off;
     off += (size_t)p.nstage_k * L.kstage;
@@ -98,7 +100,7 @@ __host__ __device__ inline FastLayout fast_layout(const SplitParams& p, int nlim
     L.qscale = off;
     off += fl_round(NQ * NBH * 4, 16);
     L.S = off;
-    off += fl_round(2 * NQ * kFastRows * 4, 16);
+    off += fl_round((size_t)kFastSDepth * NQ * kFastRows * 4, 16);
     L.P = off;
     off += fl_round(2 * (size_t)kFastRows * (NQ + 4) * 4, 16);
     L.alpha = off;
@@ -108,8 +110,7 @@ __host__ __device__ inline FastLayout fast_layout(const SplitParams& p, int nlim
     L.lrun = off;
     off += fl_round(NQ * 4, 16);
     L.red = off;
-    const size_t red_floats = (rpV > 1 ? rpV - 1 : 1) * (size_t)p.red_heads * p.QC * p.D;
-    off += fl_round(red_floats * 4, 16);
+    (void)rpV;
     L.lens = off;
     off += fl_round((3 * (size_t)p.B + 1) * 4, 16);
     L.bars = off;
@@ -140,9 +141,11 @@ size_t split_smem_bytes(const SplitParams& p);
 int split_max_smem();
 cudaError_t launch_split(const SplitParams& p, int grid, cudaStream_t s);
 // warp-specialised decode (kvq_decode_fast.cu): token rows must be 16-byte multiples
-cudaError_t launch_split_fast(const SplitParams& p, const CUtensorMap& kmap, int grid, cudaStream_t s);
-// 2-D TMA map of a key plane: rows x k_tok bytes, boxes of kFastRows x 128 bytes, 128-byte swizzle
-bool make_key_tensor_map(CUtensorMap* map, void* k_plane, int k_tok, long long rows);
+cudaError_t launch_split_fast(const SplitParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
+                              cudaStream_t s);
+// 3-D TMA map of a byte plane of `rows` token rows: one box = kFastRows rows x
+// all 128-byte column blocks, 128-byte swizzle
+bool make_row_tensor_map(CUtensorMap* map, void* plane, int tok_bytes, long long rows);
 cudaError_t launch_merge(const MergeParams& p, int T, int max_splits, bool pdl, cudaStream_t s);
 
 }  // namespace kvq

@@ -49,16 +49,18 @@ def test_bytes_per_token_and_required_sizes(L):
     # kb = 8*128/32 = 32 blocks: 32*34 + 32*24 = 1856 bytes per token
     assert B.kvq_bytes_per_token(cfg) == 1856
     sz = B.kvq_required_bytes(cfg)
-    assert sz.k_plane == 32768 * 1088
-    assert sz.v_plane == 32768 * 768
+    # plus one 128-byte column block of padding, rounded up to 256 bytes
+    assert sz.k_plane == 32768 * 1088 + 256
+    assert sz.v_plane == 32768 * 768 + 256
     assert sz.counters >= (2 * 1 + 1) * 4 and sz.counters % 256 == 0
     assert sz.workspace > 0
     ring = B.make_config(1, 8, 64, 64, max_t=1, window=4096, ring=1)
     sz = B.kvq_required_bytes(ring)
     # ring of window + 31 rows at T = 1
-    # planes are rounded up to 256 bytes so aligned tile copies stay inside
-    assert sz.k_plane == -(-4127 * 16 * 34 // 256) * 256
-    assert sz.v_plane == -(-4127 * 16 * 24 // 256) * 256
+    # planes are padded by one 128-byte column block and rounded up to 256
+    # bytes so whole-block tile copies stay inside
+    assert sz.k_plane == -(-(4127 * 16 * 34 + 128) // 256) * 256
+    assert sz.v_plane == -(-(4127 * 16 * 24 + 128) // 256) * 256
 
 
 @pytest.mark.parametrize("kw,status", [

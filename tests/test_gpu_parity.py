@@ -99,7 +99,8 @@ def test_append_t512_equals_512_single_rows():
         a.append(kd[t0:t0 + 64].unsqueeze(0), vd[t0:t0 + 64].unsqueeze(0))
     for t in range(512):
         b.append(kd[t:t + 1].unsqueeze(0), vd[t:t + 1].unsqueeze(0))
-    assert torch.equal(a.k_plane, b.k_plane) and torch.equal(a.v_plane, b.v_plane)
+    assert torch.equal(a.k_rows(0, 0, 512), b.k_rows(0, 0, 512))
+    assert torch.equal(a.v_rows(0, 0, 512), b.v_rows(0, 0, 512))
     ora = O.OracleKvCache(1, wl.n_kv, wl.head_dim)
     ora.append(k.unsqueeze(0).numpy(), v.unsqueeze(0).numpy())
     assert_rows_equal(a, ora, 0, 0, 512)
