@@ -178,8 +178,10 @@ kvq_status kvq_physical_rows(const kvq_cache* cache, int seq, int start,
 kvq_status kvq_read_device_error(kvq_cache* cache, int* err, void* stream);
 
 /* Choose the decode kernel: path 0 = automatic (the warp-specialised kernel
- * whenever token rows are 16-byte multiples and its tiles fit shared memory,
- * else the generic split kernel), 1 = generic, 2 = warp-specialised
+ * whenever token rows are 16-byte multiples, n_kv_heads <= 8,
+ * (queries per KV head rounded up to 4 or 8) / 4 * n_kv_heads * head_dim / 32
+ * is a power of two <= 128, and its tiles fit shared memory, else the generic
+ * split kernel), 1 = generic, 2 = warp-specialised
  * (KVQ_EUNSUPPORTED at decode time if the geometry does not allow it).
  * query_bits (0 = 24, or 16): the warp-specialised kernel quantises each
  * pre-scaled query element per 32-element block to this many bits against

@@ -309,8 +309,11 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
     const int NBH = D / 32;
     const int nK = (QC / 4) * Hkv * NBH;
     const bool generic_ok = 2 * nK <= kSplitThreads && kSplitThreads % (2 * nK) == 0;
-    // the warp-specialised kernel needs 16-byte token rows and at most 256 V tasks per row
-    bool fast = c->path != 1 && c->kmap_ok && 2 * nK <= 256 && (2 * nK) % 8 == 0 && Hkv <= 8;
+    // the warp-specialised kernel needs 16-byte token rows
+    // (value tasks per row: a power of two from 8 to 256, so each V warp holds
+    // a power-of-two number of tasks and its row groups reduce by butterfly)
+    bool fast = c->path != 1 && c->kmap_ok && 2 * nK >= 8 && 2 * nK <= 256 && ((2 * nK) & (2 * nK - 1)) == 0 &&
+                Hkv <= 8;
     if (!fast && !generic_ok)
         return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
     long long total_vis = 0;
@@ -328,6 +331,7 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
     const int max_splits = (c->max_vis + C - 1) / C;
 
     SplitParams p;
+    p.q_stage = 0;
     p.k_plane = c->k_plane;
     p.v_plane = c->v_plane;
     p.len_d = c->len_d;
@@ -370,10 +374,15 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
         bool fits = false;
         const int depths[4][2] = {{3, 3}, {3, 2}, {2, 3}, {2, 2}};
         p.red_heads = 1;
-        for (int di = 0; di < 4 && !fits; ++di) {
-            p.nstage_k = depths[di][0];
-            p.nstage_v = depths[di][1];
-            fits = fast_layout(p, p.nlimb).total <= (size_t)smem_max;
+        // stage next-item queries in shared memory when there is room and the
+        // query rows are 16-byte aligned
+        for (int stage_q = ((uintptr_t)q % 16 == 0) ? 1 : 0; stage_q >= 0 && !fits; --stage_q) {
+            p.q_stage = stage_q;
+            for (int di = 0; di < 4 && !fits; ++di) {
+                p.nstage_k = depths[di][0];
+                p.nstage_v = depths[di][1];
+                fits = fast_layout(p, p.nlimb).total <= (size_t)smem_max;
+            }
         }
         if (!fits) fast = false;
     }

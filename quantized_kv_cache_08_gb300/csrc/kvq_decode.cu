@@ -468,32 +468,59 @@ __global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitPara
 
 // Merge the partials of one (sequence, query) over its splits, with the sink:
 // M = max(sink, m_s), L = 2^(sink-M) + sum l_s 2^(m_s-M), out = sum o_s 2^(m_s-M) / L
-// (all in log2 units).  CTA = (query record, sequence, 32-dim chunk); each warp
-// folds every 8th split into a running (max, sum, o) with loads issued four
-// splits ahead, then the eight warp states are combined once.
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
-    constexpr int NW = kMergeThreads / 32;
-    const int gq = blockIdx.x;                      // t * Hq + h
+// (all in log2 units).  CTA = (group of QPB query records, sequence); its
+// warps are QPB x SW: warp (qi, sg) folds splits sg, sg + SW, ... of query qi
+// into a running (max, sum, o) with U splits' loads in flight, each lane
+// holding VPL = D/32 consecutive dims (one vector load per split); the SW
+// warp states of a query are then combined once through shared memory.
+// largest merge CTA for VPL values per lane (registers: U splits of VPL in flight)
+__host__ __device__ constexpr int merge_threads(int vpl) { return vpl <= 2 ? kMergeThreads : vpl <= 8 ? 512 : 256; }
+
+template <int VPL>
+__global__ void __launch_bounds__(merge_threads(VPL)) merge_kernel(const MergeParams p, int QPB, int SW) {
+    constexpr int U = VPL >= 8 ? 4 : 8;             // splits whose loads are in flight together
+    extern __shared__ float msm[];                  // [QPB][SW][2 + D]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qi = warp % QPB, sg = warp / QPB;
+    const int gq = blockIdx.x * QPB + qi;           // t * Hq + h
     const int b = blockIdx.y;
-    const int dim = blockIdx.z * 32 + (threadIdx.x & 31);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int D = VPL * 32;
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    const bool live = gq < p.Qtot;
     const int first = p.plan[b];
-    const int ns = p.plan[b + 1] - first;
+    const int ns = live ? p.plan[b + 1] - first : 0;
     const float* ml = p.part_ml + ((long long)first * p.Qtot + gq) * 2;
-    const float* po = p.part_o + ((long long)first * p.Qtot + gq) * p.D + dim;
+    const float* po = p.part_o + ((long long)first * p.Qtot + gq) * D + lane * VPL;
     const long long rs = (long long)p.Qtot;        // record stride between splits
-    float M = kNegInf, L = 0.f, acc = 0.f;
-    constexpr int U = 8;                            // splits whose loads are in flight together
-    for (int s0 = warp; s0 < ns; s0 += U * NW) {
-        float m4[U], l4[U], o4[U];
+    float M = kNegInf, L = 0.f, acc[VPL];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) acc[v] = 0.f;
+    for (int s0 = sg; s0 < ns; s0 += U * SW) {
+        float m4[U], l4[U], o4[U][VPL];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int s = s0 + u * NW;
+            const int s = s0 + u * SW;
             const bool ok = s < ns;
-            m4[u] = ok ? ml[s * rs * 2] : kNegInf;
-            l4[u] = ok ? ml[s * rs * 2 + 1] : 0.f;
-            o4[u] = ok ? po[s * rs * p.D] : 0.f;
+            const float2 mlv = ok ? *reinterpret_cast<const float2*>(ml + s * rs * 2) : make_float2(kNegInf, 0.f);
+            m4[u] = mlv.x;
+            l4[u] = mlv.y;
+            const float* src = po + s * rs * D;
+            if constexpr (VPL % 4 == 0) {
+#pragma unroll
+                for (int v = 0; v < VPL; v += 4) {
+                    const float4 x = ok ? *reinterpret_cast<const float4*>(src + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    o4[u][v] = x.x;
+                    o4[u][v + 1] = x.y;
+                    o4[u][v + 2] = x.z;
+                    o4[u][v + 3] = x.w;
+                }
+            } else if constexpr (VPL == 2) {
+                const float2 x = ok ? *reinterpret_cast<const float2*>(src) : make_float2(0.f, 0.f);
+                o4[u][0] = x.x;
+                o4[u][1] = x.y;
+            } else {
+                o4[u][0] = ok ? src[0] : 0.f;
+            }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -502,33 +529,40 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
             const float a = (M == kNegInf) ? 0.f : exp2f(M - Mn);
             const float w = exp2f(m4[u] - Mn);
             L = L * a + l4[u] * w;
-            acc = acc * a + o4[u] * w;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) acc[v] = acc[v] * a + o4[u][v] * w;
             M = Mn;
         }
     }
-    __shared__ float sM[NW], sL[NW], sA[NW][32];
+    float* st = msm + (size_t)(qi * SW + sg) * (2 + D);
     if (lane == 0) {
-        sM[warp] = M;
-        sL[warp] = L;
+        st[0] = M;
+        st[1] = L;
     }
-    sA[warp][lane] = acc;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) st[2 + lane * VPL + v] = acc[v];
     __syncthreads();
-    if (warp == 0) {
+    if (sg == 0 && live) {
         const float LOG2E = 1.4426950408889634f;
         const float sink = p.sinks ? p.sinks[gq % p.Hq] * LOG2E : kNegInf;
+        const float* q0 = msm + (size_t)qi * SW * (2 + D);
         float Mt = sink;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) Mt = fmaxf(Mt, sM[w]);
+        for (int w = 0; w < SW; ++w) Mt = fmaxf(Mt, q0[w * (2 + D)]);
         float Lt = (sink == kNegInf) ? 0.f : exp2f(sink - Mt);
-        float At = 0.f;
+        float At[VPL];
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            if (sM[w] == kNegInf) continue;
-            const float f = exp2f(sM[w] - Mt);
-            Lt += sL[w] * f;
-            At += sA[w][lane] * f;
+        for (int v = 0; v < VPL; ++v) At[v] = 0.f;
+        for (int w = 0; w < SW; ++w) {
+            const float* e = q0 + w * (2 + D);
+            if (e[0] == kNegInf) continue;
+            const float f = exp2f(e[0] - Mt);
+            Lt += e[1] * f;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) At[v] += e[2 + lane * VPL + v] * f;
         }
-        p.out[(((long long)b * p.Qtot) + gq) * p.D + dim] = At / Lt;
+        float* dst = p.out + (((long long)b * p.Qtot) + gq) * D + lane * VPL;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) dst[v] = At[v] / Lt;
     }
 }
 
@@ -576,16 +610,26 @@ cudaError_t launch_split(const SplitParams& p, int grid, cudaStream_t s) {
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_merge(const MergeParams& p, int T, int max_splits, bool pdl, cudaStream_t s) {
-    (void)max_splits;
-    const size_t smem = 0;
+template <int VPL>
+cudaError_t launch_merge_t(const MergeParams& p, int max_splits, bool pdl, cudaStream_t s) {
+    // split warps per query: enough that each folds about four splits, up
+    // to a whole CTA; queries per CTA fill the remaining warps
+    constexpr int NW = merge_threads(VPL) / 32;
+    int SW = 1;
+    while (SW < NW && SW * 4 < max_splits) SW *= 2;
+    int QPB = 1;
+    while (QPB * 2 * SW <= NW && QPB * 2 <= p.Qtot) QPB *= 2;
+    const size_t smem = (size_t)QPB * SW * (2 + VPL * 32) * sizeof(float);
+    auto fn = merge_kernel<VPL>;
     // same shared-memory carveout as the split kernels, so merge CTAs launched
     // early (programmatic dependent launch) can wait beside the split CTAs
-    cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.Hq * T), (unsigned)p.B, (unsigned)(p.D / 32));
-    cfg.blockDim = dim3(kMergeThreads);
+    cfg.gridDim = dim3((unsigned)((p.Qtot + QPB - 1) / QPB), (unsigned)p.B, 1);
+    cfg.blockDim = dim3((unsigned)(32 * QPB * SW));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -593,9 +637,21 @@ cudaError_t launch_merge(const MergeParams& p, int T, int max_splits, bool pdl, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, merge_kernel, p);
+    e = cudaLaunchKernelEx(&cfg, fn, p, QPB, SW);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const MergeParams& p, int T, int max_splits, bool pdl, cudaStream_t s) {
+    (void)T;
+    switch (p.D / 32) {
+        case 1: return launch_merge_t<1>(p, max_splits, pdl, s);
+        case 2: return launch_merge_t<2>(p, max_splits, pdl, s);
+        case 4: return launch_merge_t<4>(p, max_splits, pdl, s);
+        case 8: return launch_merge_t<8>(p, max_splits, pdl, s);
+        case 16: return launch_merge_t<16>(p, max_splits, pdl, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace kvq

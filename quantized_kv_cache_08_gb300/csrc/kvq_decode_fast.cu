@@ -4,36 +4,38 @@
 // cortiq-engine "Struct LayerKvCache" fn attend_group_upto (window, causal
 // upto, sinks, GQA) over memra-engine "Struct KvLayer" q8_0 / q5_1 rows.
 //
-// A CTA has 16 warps.  Warps 0-7 (K warps) only turn key rows into scores;
-// warps 8-15 (V warps) issue every copy, run the online softmax and
-// accumulate p * v_hat.  The two sides work on different tiles at once: the
-// K warps may run two 32-row tiles ahead, with two score / probability
-// buffers handed over through named barriers (bar.arrive / bar.sync).  Key
-// bytes land in padded row slots through 16-byte cp.async copies tracked by
-// an mbarrier (cp.async.mbarrier.arrive); value bytes of a tile arrive by one
-// 1-D bulk TMA copy (cp.async.bulk) on its own mbarrier ring.
+// A CTA has 16 warps.  The key and the value bytes of a 32-row tile each
+// arrive by one 3-D TMA copy (cp.async.bulk.tensor, 32 rows x all 128-byte
+// column blocks, 128-byte swizzle) into its own ring of stages.  The last of
+// the 8 warps that read a stage (a shared-memory counter decides) issues the
+// copy that refills it, with the row coordinate from a small look-ahead table
+// that K warp 0 keeps filled, so no warp waits to issue copies.  Warps 0-7
+// (K warps) turn key rows into scores and run the online softmax; warps 8-15
+// (V warps) accumulate p * v_hat.  Probabilities
+// pass from K to V warps through a ring of kPDepth buffers handed over with
+// named barriers (bar.arrive / bar.sync), so the K warps may run up to
+// kPDepth tiles ahead.
 //
-// K warps: lane = token row.  The swizzle puts the same 16-byte column of 8
-// consecutive rows in 8 different bank groups, so the 32 lanes read their
-// rows with conflict-free 16-byte loads.  The query is
-// pre-scaled by scale * log2 e, quantised per (query, 32-element block) to
-// NLIMB*8 bits against the block's largest magnitude (24 bits: the error is
-// at the level of fp32 rounding) and split into int8 limbs held in shared
-// memory; every lane reads the same limb words (broadcast).  DP4A multiplies
-// four int8 codes by four limb bytes and accumulates in int32, so the codes
-// are never converted to float; per block the limb sums are combined in
-// float and scaled by d_k * s_q.
-//
-// V warps, softmax: a warp owns every 8th query of the CTA; lane = row.  The
-// reference maximum moves only when a score exceeds it by more than 8 (log2
-// units); a warp vote finds that rare case, otherwise p = 2^(s - m_ref) needs
-// no reduction and each lane keeps a partial sum of p until the item ends.
-// V warps, accumulation: a task is (query group of 4, KV head, block, half
-// block); a warp holds TW consecutive tasks and 32/TW lane groups that take
-// interleaved rows, so the row partial sums reduce with warp shuffles at the
-// end of an item.  The 5-bit codes are rebuilt with byte arithmetic and placed
-// in the mantissa of 0.5 (value 0.5 + u/256), so v_hat = 256 d F + (m - 128 d)
-// and o += (256 p d) F with packed FMAs, plus sum p (m - 128 d) per block.
+// K warps: lane = token row; a warp owns whole (KV head, query group of 4)
+// units.  The swizzle puts the same 16-byte column of 8 consecutive rows in 8
+// different bank groups, so the 32 lanes read their rows with conflict-free
+// 16-byte loads.  The query is pre-scaled by scale * log2 e, quantised per
+// (query, 32-element block) to NLIMB*8 bits against the block's largest
+// magnitude and split into int8 limbs held in shared memory; every lane reads
+// the same limb words (broadcast).  DP4A multiplies four int8 codes by four
+// limb bytes and accumulates in int32, so the codes are never converted to
+// float; per block the limb sums are combined in float and scaled by d_k * s_q.
+// Softmax: the unit's scores of a tile sit one row per lane, so the reference
+// maximum is a warp reduction.  It moves only when a score exceeds it by more
+// than 8 (log2 units); a warp vote finds that rare case, otherwise
+// p = 2^(s - m_ref) needs no reduction and each lane keeps a partial sum of p
+// until the item ends.
+// V warps: a task is (query group of 4, KV head, block, half block); a warp
+// holds TW consecutive tasks and 32/TW lane groups that take interleaved
+// rows, so the row partial sums reduce with warp shuffles at the end of an
+// item.  The 5-bit codes are rebuilt with byte arithmetic and placed in the
+// mantissa of 0.5 (value 0.5 + u/256), so v_hat = 256 d F + (m - 128 d) and
+// o += (256 p d) F with packed FMAs, plus sum p (m - 128 d) per block.
 #include "kvq_device.cuh"
 
 namespace kvq {
@@ -43,9 +45,11 @@ using namespace dev;
 
 constexpr int kThreads = kFastThreads;
 constexpr int kRows = kFastRows;
-constexpr int kSDepth = kFastSDepth;               // score buffers between K and V warps
+constexpr int kPDepth = kFastPDepth;           // probability buffers between K and V warps
 constexpr int kKThreads = 256;                 // warps 0-7
-constexpr int BAR_K = 1, BAR_V = 2, BAR_QLOAD = 3, BAR_FULL = 4, BAR_EMPTY = 4 + kSDepth;
+constexpr int kKVThreads = 512;                // K and V warps
+constexpr int kYRing = 16;                     // look-ahead table of tile row coordinates
+constexpr int BAR_K = 1, BAR_FULL = 2, BAR_EMPTY = 2 + kPDepth;
 constexpr long long kWaitCycles = 1LL << 31;   // ~1 s bound on any mbarrier wait
 
 __device__ __forceinline__ void bar_sync(int id, int n) {
@@ -83,6 +87,15 @@ __device__ __forceinline__ int dp4a_ss(unsigned a, unsigned b, int c) {   // a, 
     int d;
     asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
+}
+
+// Quotient and remainder of 0 <= a < 2^20 by 1 <= b <= 1024 through a float
+// reciprocal: (a + 0.5) / b lies at least 0.5 / b from an integer and the
+// float product is off by less than 0.13 / b there, so truncation is exact.
+__device__ __forceinline__ int qdiv(int a, int b, float inv_b, int& rem) {
+    const int q = __float2int_rz(((float)a + 0.5f) * inv_b);
+    rem = a - q * b;
+    return q;
 }
 
 // Bounded wait that gives up for the whole CTA once any wait has run out: the
@@ -283,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                                                             const __grid_constant__ CUtensorMap vmap) {
     constexpr int QC = 4 * NQG;
     constexpr int D = NBH * 32;
-    constexpr int NQMAX = 32 * NQG;                 // CTA queries (Hkv * QC, Hkv <= 8): <= 4 * NQG per softmax warp
+    constexpr int UPW = NQG;                        // units (KV head, query group) per K warp at most (Hkv <= 8)
     extern __shared__ __align__(128) uint8_t smem_raw[];
     // swizzled TMA boxes need a 1024-byte aligned destination
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -292,25 +305,28 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
     const int warp = tid >> 5, lane = tid & 31;
     const int Hkv = p.Hkv;
     const int NQ = Hkv * QC;
-    const int PS = NQ + 4;                          // row stride of the probability buffer
+    const int PS = NQ + 4;                          // row stride of a probability buffer
+    const float inv_hpk = 1.f / (float)p.hpk;
 
     uint8_t* kring = smem + L.kring;
     uint8_t* vring = smem + L.vring;
     uint32_t* qlimb = reinterpret_cast<uint32_t*>(smem + L.qlimb);
     float* qscl = reinterpret_cast<float*>(smem + L.qscale);
-    float* S = reinterpret_cast<float*>(smem + L.S);            // [kSDepth][NQ][kRows]
-    float* P = reinterpret_cast<float*>(smem + L.P);            // [2][kRows][PS]
-    float* alpha = reinterpret_cast<float*>(smem + L.alpha);    // [2][NQ]
+    uint8_t* qraw = smem + L.qraw;
+    float* P = reinterpret_cast<float*>(smem + L.P);            // [kPDepth][kRows][PS]
+    float* alpha = reinterpret_cast<float*>(smem + L.alpha);    // [kPDepth][NQ]
     int* qlo = reinterpret_cast<int*>(smem + L.mrun);           // [NQ] first visible row per CTA query
     int* qup = reinterpret_cast<int*>(smem + L.lrun);           // [NQ] one past the last (-1: no query)
     int* lens = reinterpret_cast<int*>(smem + L.lens);
     int* bases = lens + p.B;
     int* prefix = bases + p.B;
-    uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + L.bars);
-    uint64_t* vbar = kbar + p.nstage_k;
+    uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* vfull = kfull + p.nstage_k;
     __shared__ int s_abort;
-    __shared__ Cursor s_kc, s_vc;                   // copy producer state (V thread 0 only)
-    __shared__ int s_k_issued, s_v_issued;
+    __shared__ int4 s_tinfo[kPDepth];               // per probability buffer: rows, last, query slice, record (-1 rows: end)
+    __shared__ int s_y[kYRing];                     // row coordinate of tile j in the planes' maps (-1: no tile j)
+    __shared__ int s_kcnt[4], s_vcnt[4];            // releases per key / value stage (8 per use)
+    __shared__ Cursor s_ahead;                      // thread 0's look-ahead cursor
 
     for (int b = tid; b < p.B; b += kThreads) {
         lens[b] = p.len_d[b];
@@ -320,8 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
     __syncthreads();
     if (warp == 0) plan_splits(p, lens, bases, prefix, lane);
     if (tid == 0) {
-        for (int s2 = 0; s2 < p.nstage_k; ++s2) mbar_init(smem_u32(&kbar[s2]), 1);
-        for (int s2 = 0; s2 < p.nstage_v; ++s2) mbar_init(smem_u32(&vbar[s2]), 1);
+        for (int s2 = 0; s2 < p.nstage_k; ++s2) mbar_init(smem_u32(&kfull[s2]), 1);
+        for (int s2 = 0; s2 < p.nstage_v; ++s2) mbar_init(smem_u32(&vfull[s2]), 1);
+        for (int s2 = 0; s2 < 4; ++s2) s_kcnt[s2] = s_vcnt[s2] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -333,11 +350,36 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if ((int)blockIdx.x >= n_items) return;
 
+    const uint32_t kring_a = smem_u32(kring), vring_a = smem_u32(vring);
+    const uint32_t kfull_a = smem_u32(kfull), vfull_a = smem_u32(vfull);
+    const uint32_t kstage_b = (uint32_t)L.kstage, vstage_b = (uint32_t)L.vstage;
+    const int nsk = p.nstage_k, nsv = p.nstage_v;
+    const CUtensorMap* kmap_p = &kmap;
+    const CUtensorMap* vmap_p = &vmap;
+    auto issue_k = [=](int j, int y) {
+        const uint32_t st = (uint32_t)(j % nsk);
+        mbar_expect_tx(kfull_a + 8u * st, kstage_b);
+        tma_load_rows(kring_a + st * kstage_b, kmap_p, y, kfull_a + 8u * st);
+    };
+    auto issue_v = [=](int j, int y) {
+        const uint32_t st = (uint32_t)(j % nsv);
+        mbar_expect_tx(vfull_a + 8u * st, vstage_b);
+        tma_load_rows(vring_a + st * vstage_b, vmap_p, y, vfull_a + 8u * st);
+    };
+    const int LA = max(p.nstage_k, p.nstage_v);     // look-ahead of the row table
+
     if (warp < 8) {
         // ======================================================== K warps
-        // lane = token row of the tile; each warp scores whole (head, query
-        // group) units and hands the scores over to the V warps.
         const int kt = tid;
+        float m_ref[UPW][4], lsum[UPW][4];
+#pragma unroll
+        for (int u = 0; u < UPW; ++u)
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                m_ref[u][n] = kNegInf;
+                lsum[u][n] = 0.f;
+            }
+        const int nunit = Hkv * NQG;
         Cursor c = cursor_begin(p, lens, bases, prefix, n_items);
         int jt = 0;
         while (c.item < n_items) {
@@ -345,8 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
             if (ti.first) {
                 // quantise this item's pre-scaled queries into int8 limbs: one
                 // thread per 4 consecutive dims of a query, the 8 threads of a
-                // 32-dim block share its largest magnitude through shuffles
-                bar_sync(BAR_K, kKThreads);          // previous item's scores are done
+                // 32-dim block share its largest magnitude through shuffles.
+                // Later items read queries staged in shared memory during the
+                // item before (cp.async), the first item reads global memory.
+                const bool staged = p.q_stage && jt > 0;
+                if (staged) asm volatile("cp.async.wait_all;" ::: "memory");
+                bar_sync(BAR_K, kKThreads);          // previous item's scores are done; staged queries in
                 const int nunits = NQ * (D / 4);
                 constexpr int QB = 4;                // units per thread whose loads are in flight together
                 for (int u0 = 0; u0 < nunits; u0 += QB * kKThreads) {
@@ -359,8 +405,23 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                         const int qi = ti.it.qs * QC + ql;
 #pragma unroll
                         for (int e = 0; e < 4; ++e) xs[j][e] = 0.f;
-                        if (u < nunits && qi < p.hpk * p.T) {
-                            const int t = qi / p.hpk, h = g * p.hpk + qi % p.hpk;
+                        if (u < nunits && qi < p.hpk * p.T && staged) {
+                            if (p.q_bf16) {
+                                const uint2 raw = *reinterpret_cast<const uint2*>(qraw + ((size_t)qq * D + 4 * w4) * 2);
+                                xs[j][0] = __uint_as_float(raw.x << 16);
+                                xs[j][1] = __uint_as_float(raw.x & 0xffff0000u);
+                                xs[j][2] = __uint_as_float(raw.y << 16);
+                                xs[j][3] = __uint_as_float(raw.y & 0xffff0000u);
+                            } else {
+                                const float4 f = *reinterpret_cast<const float4*>(qraw + ((size_t)qq * D + 4 * w4) * 4);
+                                xs[j][0] = f.x;
+                                xs[j][1] = f.y;
+                                xs[j][2] = f.z;
+                                xs[j][3] = f.w;
+                            }
+                        } else if (u < nunits && qi < p.hpk * p.T) {
+                            int hr;
+                            const int t = qdiv(qi, p.hpk, inv_hpk, hr), h = g * p.hpk + hr;
                             const long long base = ((long long)(ti.b * p.T + t) * p.Hq + h) * D + 4 * w4;
                             if (p.q_bf16) {
                                 const uint2 raw = *reinterpret_cast<const uint2*>(
@@ -379,9 +440,25 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                             }
                         }
                     }
-                    // the first item's query loads go out ahead of the tile stream:
-                    // the copy producer waits for this signal before its first copies
-                    if (jt == 0 && u0 == 0) bar_arrive(BAR_QLOAD, kKThreads + 32);
+                    if (jt == 0 && u0 == 0 && tid == 0) {
+                        // the first query loads are out, ahead of the tile stream:
+                        // thread 0 starts a cursor LA tiles ahead (kept in shared
+                        // memory for the row table) and issues the first copies,
+                        // tile 0's key and value first
+                        Cursor ahead = cursor_begin(p, lens, bases, prefix, n_items);
+                        for (int j2 = 0; j2 < LA; ++j2) {
+                            int y = -1;
+                            if (ahead.item < n_items) {
+                                const TileInfo ta = tile_of(ahead);
+                                y = ta.b * p.max_rows + (ta.r0 - ta.base);
+                                advance(ahead, ta, p, lens, bases, prefix, n_items);
+                            }
+                            s_y[j2] = y;
+                            if (y >= 0 && j2 < p.nstage_k) issue_k(j2, y);
+                            if (y >= 0 && j2 < p.nstage_v) issue_v(j2, y);
+                        }
+                        s_ahead = ahead;
+                    }
 #pragma unroll
                     for (int j = 0; j < QB; ++j) {
                         const int u = u0 + j * kKThreads + kt;
@@ -397,7 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
 #pragma unroll
                         for (int o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                         constexpr float QMAX = NLIMB == 3 ? 8388607.f : 32767.f;
-                        const float inv = mx > 0.f ? QMAX / mx : 0.f;
+                        // any scale works here: the dot products are rescaled by mx / QMAX
+                        const float inv = mx > 0.f ? __fdividef(QMAX, mx) : 0.f;
                         int v4[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -415,106 +493,175 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                                 for (int e = 0; e < 4; ++e) word |= (uint32_t)((v4[e] >> (8 * l)) & 0xff) << (8 * e);
                                 dst[l * 4 + n] = word;
                             }
-                            if (k == 0) qscl[(unit * NBH + bi) * 4 + n] = mx / QMAX;
+                            if (k == 0) qscl[(unit * NBH + bi) * 4 + n] = mx * (1.f / QMAX);
                         }
                     }
                 }
                 for (int qq = kt; qq < NQ; qq += kKThreads) {
                     const int qi = ti.it.qs * QC + qq % QC;
                     const bool valid = qi < p.hpk * p.T;
-                    const int upto = ti.len - p.T + (valid ? qi / p.hpk : 0) + 1;
+                    int hr;
+                    const int upto = ti.len - p.T + (valid ? qdiv(qi, p.hpk, inv_hpk, hr) : 0) + 1;
                     qup[qq] = valid ? upto : -1;
                     qlo[qq] = p.window > 0 ? max(0, upto - p.window) : 0;
                 }
                 bar_sync(BAR_K, kKThreads);          // limbs and row windows visible to every K warp
+                if (p.q_stage && c.item + (int)gridDim.x < n_items) {
+                    // stage the next item's raw queries: 16-byte cp.async
+                    // chunks of each query row (rows of absent queries skipped)
+                    const Item nx = item_of(c.item + (int)gridDim.x, prefix, p.B, p.nqs);
+                    const int esz = p.q_bf16 ? 2 : 4;
+                    const int cpr = D * esz / 16;    // chunks per query row
+                    for (int ch = kt; ch < NQ * cpr; ch += kKThreads) {
+                        const int qq = ch / cpr, k16 = ch - qq * cpr;
+                        const int g = qq / QC, qi = nx.qs * QC + qq % QC;
+                        if (qi < p.hpk * p.T) {
+                            int hr;
+                            const int t = qdiv(qi, p.hpk, inv_hpk, hr), h = g * p.hpk + hr;
+                            const char* src = reinterpret_cast<const char*>(p.q) +
+                                              (((long long)(nx.b * p.T + t) * p.Hq + h) * D) * esz + 16 * k16;
+                            const uint32_t dst = smem_u32(qraw + ((size_t)qq * D) * esz + 16 * k16);
+                            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+                        }
+                    }
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                }
+            }
+            if (tid == 0) {
+                // row coordinate of tile jt + LA, before this warp's release below
+                Cursor ahead = s_ahead;
+                int y = -1;
+                if (ahead.item < n_items) {
+                    const TileInfo ta = tile_of(ahead);
+                    y = ta.b * p.max_rows + (ta.r0 - ta.base);
+                    advance(ahead, ta, p, lens, bases, prefix, n_items);
+                }
+                s_y[(jt + LA) % kYRing] = y;
+                s_ahead = ahead;
             }
             // ------------------------------------------------ scores
             const int kst = jt % p.nstage_k;
-            wait_stage(smem_u32(&kbar[kst]), (uint32_t)((jt / p.nstage_k) & 1), &s_abort, p.err_d);
+            wait_stage(smem_u32(&kfull[kst]), (uint32_t)((jt / p.nstage_k) & 1), &s_abort, p.err_d);
             const uint32_t kbase = smem_u32(kring + (size_t)kst * L.kstage);
             const uint32_t rowoff = (uint32_t)lane * 128u, sw = (uint32_t)lane & 7u;
-            const int sb = jt % kSDepth;
-            if (jt >= kSDepth) bar_sync(BAR_EMPTY + sb, kThreads);  // V has read the scores of tile jt-kSDepth
-            float* Sb = S + sb * NQ * kRows;
             const int row = ti.r0 + lane;
-#pragma unroll 1
-            for (int unit = warp; unit < Hkv * NQG; unit += 8) {
-                const int g = unit / NQG, qg = unit - g * NQG;
-                float sc[4] = {0.f, 0.f, 0.f, 0.f};
-                if (lane < ti.nr) {
+            float sc[UPW][4];
+#pragma unroll
+            for (int u = 0; u < UPW; ++u) {
+                const int unit = warp + 8 * u;
+#pragma unroll
+                for (int n = 0; n < 4; ++n) sc[u][n] = 0.f;
+                if (unit < nunit && lane < ti.nr) {
+                    const int g = unit / NQG;
                     const uint32_t ql_unit = smem_u32(qlimb + (size_t)(unit * NBH) * 8 * NLIMB * 4);
                     const uint32_t qs_unit = smem_u32(qscl + (size_t)(unit * NBH) * 4);
-                    head_scores_dispatch<NBH, NLIMB>(kbase, rowoff, sw, g, ql_unit, qs_unit, sc);
-                }
-                const int qq0 = g * QC + 4 * qg;
-#pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    const bool vis = lane < ti.nr && row >= qlo[qq0 + n] && row < qup[qq0 + n];
-                    Sb[(qq0 + n) * kRows + lane] = vis ? sc[n] : kNegInf;
+                    head_scores_dispatch<NBH, NLIMB>(kbase, rowoff, sw, g, ql_unit, qs_unit, sc[u]);
                 }
             }
-            bar_arrive(BAR_FULL + sb, kThreads);           // scores of tile jt; K stage jt is free
+            __syncwarp();
+            if (lane == 0) {
+                // this warp is done with the key stage; the last of the 8 refills it
+                __threadfence_block();
+                if ((atomicAdd(&s_kcnt[kst], 1) & 7) == 7) {
+                    __threadfence_block();
+                    const int y = s_y[(jt + p.nstage_k) % kYRing];
+                    if (y >= 0 && !*(volatile int*)&s_abort) issue_k(jt + p.nstage_k, y);
+                }
+            }
+            // ------------------------------------------------ online softmax
+            const int slot = jt % kPDepth;
+            float pv[UPW][4], al[UPW][4];
+#pragma unroll
+            for (int u = 0; u < UPW; ++u) {
+                const int unit = warp + 8 * u;
+                if (unit < nunit) {
+                    const int g = unit / NQG, qg = unit - g * NQG;
+                    const int qq0 = g * QC + 4 * qg;
+#pragma unroll
+                    for (int n = 0; n < 4; ++n) {
+                        const bool vis = lane < ti.nr && row >= qlo[qq0 + n] && row < qup[qq0 + n];
+                        const float s = vis ? sc[u][n] : kNegInf;
+                        al[u][n] = 1.f;
+                        if (__any_sync(0xffffffffu, s > m_ref[u][n] + kLazy)) {
+                            // the reference maximum moves: full tile maximum
+                            float tmax = s;
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+                            al[u][n] = (m_ref[u][n] == kNegInf) ? 0.f : exp2f(m_ref[u][n] - tmax);
+                            m_ref[u][n] = tmax;
+                            lsum[u][n] *= al[u][n];
+                        }
+                        pv[u][n] = (s == kNegInf) ? 0.f : exp2f(s - m_ref[u][n]);
+                        lsum[u][n] += pv[u][n];
+                    }
+                }
+            }
+            if (jt >= kPDepth) bar_sync(BAR_EMPTY + slot, kKVThreads);   // V is done with tile jt - kPDepth
+            float* Pb = P + slot * kRows * PS;
+            float* ab = alpha + slot * NQ;
+#pragma unroll
+            for (int u = 0; u < UPW; ++u) {
+                const int unit = warp + 8 * u;
+                if (unit < nunit) {
+                    const int g = unit / NQG, qg = unit - g * NQG;
+                    const int qq0 = g * QC + 4 * qg;
+                    *reinterpret_cast<float4*>(&Pb[lane * PS + qq0]) = make_float4(pv[u][0], pv[u][1], pv[u][2], pv[u][3]);
+                    if (lane == 0) *reinterpret_cast<float4*>(&ab[qq0]) = make_float4(al[u][0], al[u][1], al[u][2], al[u][3]);
+                }
+            }
+            if (tid == 0) s_tinfo[slot] = make_int4(ti.nr, ti.last ? 1 : 0, ti.it.qs, ti.it.pidx);
+            bar_arrive(BAR_FULL + slot, kKVThreads);       // probabilities of tile jt are in
+            if (ti.last) {
+                // (max, sum) of this warp's queries for the item's partial record
+#pragma unroll
+                for (int u = 0; u < UPW; ++u) {
+                    const int unit = warp + 8 * u;
+                    if (unit < nunit) {
+                        const int g = unit / NQG, qg = unit - g * NQG;
+#pragma unroll
+                        for (int n = 0; n < 4; ++n) {
+                            float l = lsum[u][n];
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+                            const int qi = ti.it.qs * QC + 4 * qg + n;
+                            if (lane == 0 && qi < p.hpk * p.T) {
+                                int hr;
+                            const int t = qdiv(qi, p.hpk, inv_hpk, hr), h = g * p.hpk + hr;
+                                const long long rec = (long long)ti.it.pidx * p.Qtot + (long long)t * p.Hq + h;
+                                p.part_ml[rec * 2] = m_ref[u][n];
+                                p.part_ml[rec * 2 + 1] = l;
+                            }
+                            m_ref[u][n] = kNegInf;
+                            lsum[u][n] = 0.f;
+                        }
+                    }
+                }
+            }
             advance(c, ti, p, lens, bases, prefix, n_items);
             ++jt;
         }
-        for (int j = max(kSDepth, jt); j < jt + kSDepth; ++j) bar_sync(BAR_EMPTY + j % kSDepth, kThreads);
+        // copies still landing after a wait ran out must finish before the CTA ends
+        if (tid == 0 && *(volatile int*)&s_abort)
+            for (int j = max(0, jt - p.nstage_k); j < jt; ++j) {
+                const long long t0 = clock64();
+                while (!mbar_try(smem_u32(&kfull[j % p.nstage_k]), (uint32_t)((j / p.nstage_k) & 1)) &&
+                       clock64() - t0 < kWaitCycles) {
+                }
+            }
+        // end mark for the V warps, then their releases of the last tiles
+        if (jt >= kPDepth) bar_sync(BAR_EMPTY + jt % kPDepth, kKVThreads);
+        if (tid == 0) s_tinfo[jt % kPDepth] = make_int4(-1, 0, 0, 0);
+        bar_arrive(BAR_FULL + jt % kPDepth, kKVThreads);
+        for (int j = max(0, jt - kPDepth + 1); j < jt; ++j) bar_sync(BAR_EMPTY + j % kPDepth, kKVThreads);
     } else {
         // ======================================================== V warps
-        // copy issue, online softmax, p * v_hat accumulation
-        const int vt = tid - kKThreads;
         const int vw = warp - 8;
-        // key and value tiles: one 3-D TMA box each (32 rows x all column
-        // blocks, 128-byte swizzle).  V thread 0 issues; its cursors live in
-        // shared memory.
-        auto issue_k = [&]() {
-            Cursor kc = s_kc;
-            if (kc.item >= n_items) return;
-            const TileInfo ti = tile_of(kc);
-            const int st = s_k_issued % p.nstage_k;
-            const uint32_t bar = smem_u32(&kbar[st]);
-            mbar_expect_tx(bar, (uint32_t)L.kstage);
-            tma_load_rows(smem_u32(kring + (size_t)st * L.kstage), &kmap, ti.b * p.max_rows + (ti.r0 - ti.base), bar);
-            ++s_k_issued;
-            advance(kc, ti, p, lens, bases, prefix, n_items);
-            s_kc = kc;
-        };
-        auto issue_v = [&]() {
-            Cursor vc = s_vc;
-            if (vc.item >= n_items) return;
-            const TileInfo ti = tile_of(vc);
-            const int st = s_v_issued % p.nstage_v;
-            const uint32_t bar = smem_u32(&vbar[st]);
-            mbar_expect_tx(bar, (uint32_t)L.vstage);
-            tma_load_rows(smem_u32(vring + (size_t)st * L.vstage), &vmap, ti.b * p.max_rows + (ti.r0 - ti.base), bar);
-            ++s_v_issued;
-            advance(vc, ti, p, lens, bases, prefix, n_items);
-            s_vc = vc;
-        };
-        if (vw == 0) bar_sync(BAR_QLOAD, kKThreads + 32);
-        if (vt == 0) {
-            s_kc = cursor_begin(p, lens, bases, prefix, n_items);
-            s_vc = s_kc;
-            s_k_issued = 0;
-            s_v_issued = 0;
-            for (int s2 = 0; s2 < p.nstage_k; ++s2) issue_k();
-            for (int s2 = 0; s2 < p.nstage_v; ++s2) issue_v();
-        }
-
-        // softmax state: this warp owns queries qq = vw + 8 i; m_ref per query
-        // (warp-uniform), lane-partial sums of p
-        float m_ref[NQMAX / 8], lsum[NQMAX / 8];
-#pragma unroll
-        for (int i = 0; i < NQMAX / 8; ++i) {
-            m_ref[i] = kNegInf;
-            lsum[i] = 0.f;
-        }
         // accumulation task: TW tasks per warp (consecutive lanes), the warp's
-        // 32 / TW lane groups take interleaved rows of the tile, so partial
-        // sums over rows meet inside the warp and reduce with shuffles
+        // 32 / TW lane groups take interleaved rows, so partial sums over rows
+        // meet inside the warp and reduce with shuffles
         const int nV = 2 * NQG * Hkv * NBH;             // tasks per row
         const int TW = nV / 8;                          // tasks per warp
         const int RG = 32 / TW;                         // row groups (lane groups) per warp
-        // lanes past TW * RG (TW not a power of two) hold no rows
         const int v_task = vw * TW + lane % TW, v_rg = lane / TW;
         const int v_hf = v_task & 1, v_bi = (v_task >> 1) % NBH, v_g = (v_task >> 1) / NBH % Hkv;
         const int v_qg = (v_task >> 1) / (NBH * Hkv);
@@ -522,6 +669,11 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
         const int v_qq0 = v_g * QC + 4 * v_qg;
         const int col_dm = v_blk * kQ5Bytes;            // d, m, qh of the thread's block
         const int col_qs = col_dm + 8 + 8 * v_hf;       // its 8 bytes of qs
+        // tile offsets of those bytes in the thread's first two rows (rows
+        // 2 RG apart share the 128-byte swizzle phase when RG >= 4)
+        const uint32_t v_o0dm = tile_addr(0, v_rg, col_dm), v_o0qs = tile_addr(0, v_rg, col_qs);
+        const uint32_t v_o1dm = tile_addr(0, v_rg + RG, col_dm), v_o1qs = tile_addr(0, v_rg + RG, col_qs);
+        const uint32_t v_p0 = 4u * (uint32_t)(v_rg * PS + v_qq0);
         float2 o2[4][8];
         float pm[4];
 #pragma unroll
@@ -530,46 +682,18 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
 #pragma unroll
             for (int i = 0; i < 8; ++i) o2[n][i] = make_float2(0.f, 0.f);
         }
-        Cursor c = cursor_begin(p, lens, bases, prefix, n_items);
         int jt = 0;
-        while (c.item < n_items) {
-            const TileInfo ti = tile_of(c);
-            const int sb = jt % kSDepth;
-            bar_sync(BAR_FULL + sb, kThreads);             // scores of tile jt are in
-            // ------------------------------------------------ online softmax
-            const float* Sb = S + sb * NQ * kRows;
-            float* Pb = P + (jt & 1) * kRows * PS;
-            float* ab = alpha + (jt & 1) * NQ;
-#pragma unroll
-            for (int i = 0; i < NQMAX / 8; ++i) {
-                const int qq = vw + 8 * i;
-                if (qq < NQ) {
-                    const float s = Sb[qq * kRows + lane];
-                    float al = 1.f;
-                    if (__any_sync(0xffffffffu, s > m_ref[i] + kLazy)) {
-                        // the reference maximum moves: full tile maximum
-                        float tmax = s;
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-                        al = (m_ref[i] == kNegInf) ? 0.f : exp2f(m_ref[i] - tmax);
-                        m_ref[i] = tmax;
-                        lsum[i] *= al;
-                    }
-                    const float pv = (s == kNegInf) ? 0.f : exp2f(s - m_ref[i]);
-                    lsum[i] += pv;
-                    Pb[lane * PS + qq] = pv;
-                    if (lane == 0) ab[qq] = al;
-                }
-            }
-            bar_arrive(BAR_EMPTY + sb, kThreads);          // scores of tile jt consumed
-            bar_sync(BAR_V, kKThreads);                    // p and alpha of tile jt written; V stage jt-1 free
-            if (vt == 0) {
-                issue_k();                                 // K stage of tile jt is free (FULL passed)
-                if (jt >= 1) issue_v();                    // V stage of tile jt-1 is free (BAR_V passed)
-            }
-            // ------------------------------------------------ accumulate
+#pragma unroll 1
+        for (;; ++jt) {
+            const int slot = jt % kPDepth;
+            bar_sync(BAR_FULL + slot, kKVThreads);         // probabilities of tile jt are in
+            const int4 tinf = s_tinfo[slot];
+            if (tinf.x < 0) break;                         // the K warps' end mark
+            const int t_nr = tinf.x, t_qs = tinf.z, t_pidx = tinf.w;
+            const float* Pb = P + slot * kRows * PS;
+            const float* ab = alpha + slot * NQ;
             const int vst = jt % p.nstage_v;
-            wait_stage(smem_u32(&vbar[vst]), (uint32_t)((jt / p.nstage_v) & 1), &s_abort, p.err_d);
+            wait_stage(smem_u32(&vfull[vst]), (uint32_t)((jt / p.nstage_v) & 1), &s_abort, p.err_d);
             const uint32_t vtile = smem_u32(vring + (size_t)vst * L.vstage);
             {
                 const float4 al4 = *reinterpret_cast<const float4*>(&ab[v_qq0]);
@@ -586,117 +710,120 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                     }
                 }
                 const uint32_t pb = smem_u32(Pb);
-                for (int r = v_rg < RG ? v_rg : kRows; r < ti.nr; r += RG) {
-                    const uint2 dmqh = lds64(tile_addr(vtile, r, col_dm));
-                    const uint2 qs = lds64(tile_addr(vtile, r, col_qs));
-                    const float4 p4 = lds128f(pb + 4u * (uint32_t)(r * PS + v_qq0));
-                    const float d = h2f(dmqh.x & 0xffffu);
-                    const float m = h2f(dmqh.x >> 16);
-                    const float d256 = d * 256.f;
-                    const float mp = fmaf(-128.f, d, m);
-                    const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
-                    float2 pd[4];
-#pragma unroll
-                    for (int n = 0; n < 4; ++n) {
-                        const float t = pr[n] * d256;
-                        pd[n] = make_float2(t, t);
-                        pm[n] = fmaf(pr[n], mp, pm[n]);
-                    }
-                    const uint32_t xl = __byte_perm(dmqh.y, 0, v_hf ? 0x1111u : 0x0000u);
-                    const uint32_t xh = __byte_perm(dmqh.y, 0, v_hf ? 0x3333u : 0x2222u);
-                    uint32_t u[4];
-                    {
-                        const uint32_t sp0 = ((xl & 0x08040201u) + 0x080C0E0Fu);
-                        const uint32_t sp1 = (((xl >> 4) & 0x08040201u) + 0x080C0E0Fu);
-                        const uint32_t sp2 = ((xh & 0x08040201u) + 0x080C0E0Fu);
-                        const uint32_t sp3 = (((xh >> 4) & 0x08040201u) + 0x080C0E0Fu);
-                        u[0] = (qs.x & 0x0F0F0F0Fu) | (sp0 & 0xF0F0F0F0u);
-                        u[1] = (qs.y & 0x0F0F0F0Fu) | (sp1 & 0xF0F0F0F0u);
-                        u[2] = ((qs.x >> 4) & 0x0F0F0F0Fu) | (sp2 & 0xF0F0F0F0u);
-                        u[3] = ((qs.y >> 4) & 0x0F0F0F0Fu) | (sp3 & 0xF0F0F0F0u);
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const float2 fa = make_float2(__uint_as_float(__byte_perm(u[cc], 0x3F000000u, 0x7044u)),
-                                                      __uint_as_float(__byte_perm(u[cc], 0x3F000000u, 0x7144u)));
-                        const float2 fb = make_float2(__uint_as_float(__byte_perm(u[cc], 0x3F000000u, 0x7244u)),
-                                                      __uint_as_float(__byte_perm(u[cc], 0x3F000000u, 0x7344u)));
+                // one row of the thread's task: d, m, qh and 8 qs bytes of its
+                // block half, the row's 4 probabilities of its query group
+                auto vrow = [&](uint32_t a_dm, uint32_t a_qs, uint32_t a_p) {
+                    const uint2 dmqh = lds64(a_dm);
+                    const uint2 qs = lds64(a_qs);
+                    const float4 p4 = lds128f(a_p);
+                        const float d = h2f(dmqh.x & 0xffffu);
+                        const float m = h2f(dmqh.x >> 16);
+                        const float d256 = d * 256.f;
+                        const float mp = fmaf(-128.f, d, m);
+                        const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
+                        float2 pd[4];
 #pragma unroll
                         for (int n = 0; n < 4; ++n) {
-                            o2[n][2 * cc] = __ffma2_rn(pd[n], fa, o2[n][2 * cc]);
-                            o2[n][2 * cc + 1] = __ffma2_rn(pd[n], fb, o2[n][2 * cc + 1]);
+                            const float t = pr[n] * d256;
+                            pd[n] = make_float2(t, t);
+                            pm[n] = fmaf(pr[n], mp, pm[n]);
                         }
+                        const uint32_t xl = __byte_perm(dmqh.y, 0, v_hf ? 0x1111u : 0x0000u);
+                        const uint32_t xh = __byte_perm(dmqh.y, 0, v_hf ? 0x3333u : 0x2222u);
+                        uint32_t u[4];
+                        {
+                            const uint32_t sp0 = ((xl & 0x08040201u) + 0x080C0E0Fu);
+                            const uint32_t sp1 = (((xl >> 4) & 0x08040201u) + 0x080C0E0Fu);
+                            const uint32_t sp2 = ((xh & 0x08040201u) + 0x080C0E0Fu);
+                            const uint32_t sp3 = (((xh >> 4) & 0x08040201u) + 0x080C0E0Fu);
+                            u[0] = (qs.x & 0x0F0F0F0Fu) | (sp0 & 0xF0F0F0F0u);
+                            u[1] = (qs.y & 0x0F0F0F0Fu) | (sp1 & 0xF0F0F0F0u);
+                            u[2] = ((qs.x >> 4) & 0x0F0F0F0Fu) | (sp2 & 0xF0F0F0F0u);
+                            u[3] = ((qs.y >> 4) & 0x0F0F0F0Fu) | (sp3 & 0xF0F0F0F0u);
+                        }
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const float2 fa = make_float2(__uint_as_float(__byte_perm(u[cc], 0x3F000000u, 0x7044u)),
+                                                          __uint_as_float(__byte_perm(u[cc], 0x3F000000u, 0x7144u)));
+                            const float2 fb = make_float2(__uint_as_float(__byte_perm(u[cc], 0x3F000000u, 0x7244u)),
+                                                          __uint_as_float(__byte_perm(u[cc], 0x3F000000u, 0x7344u)));
+#pragma unroll
+                            for (int n = 0; n < 4; ++n) {
+                                o2[n][2 * cc] = __ffma2_rn(pd[n], fa, o2[n][2 * cc]);
+                                o2[n][2 * cc + 1] = __ffma2_rn(pd[n], fb, o2[n][2 * cc + 1]);
+                            }
+                        }
+                };
+                if (RG >= 4) {
+                    // rows r and r + RG of the thread alternate between two
+                    // swizzle phases, rows 2 RG apart share one
+                    uint32_t base = vtile, pa = pb + v_p0;
+                    const uint32_t pstep = 4u * (uint32_t)(RG * PS);
+                    int r = v_rg;
+                    for (; r + RG < t_nr; r += 2 * RG) {
+                        vrow(base + v_o0dm, base + v_o0qs, pa);
+                        vrow(base + v_o1dm, base + v_o1qs, pa + pstep);
+                        base += (uint32_t)(2 * RG * 128);
+                        pa += 2 * pstep;
                     }
+                    if (r < t_nr) vrow(base + v_o0dm, base + v_o0qs, pa);
+                } else {
+                    for (int r = v_rg; r < t_nr; r += RG)
+                        vrow(tile_addr(vtile, r, col_dm), tile_addr(vtile, r, col_qs),
+                             pb + 4u * (uint32_t)(r * PS + v_qq0));
                 }
             }
-            if (ti.last) {
-                // row-group partial sums meet inside the warp: tree-reduce
-                // down the lane groups, lane group 0 ends with the sum
-                for (int st = 1; st < RG; st <<= 1) {
-                    const bool take = v_rg + st < RG;
-                    const int dl = st * TW;
-#pragma unroll
-                    for (int n = 0; n < 4; ++n) {
-                        const float a = __shfl_down_sync(0xffffffffu, pm[n], dl);
-                        if (take) pm[n] += a;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float x = __shfl_down_sync(0xffffffffu, o2[n][i].x, dl);
-                            const float y = __shfl_down_sync(0xffffffffu, o2[n][i].y, dl);
-                            if (take) {
-                                o2[n][i].x += x;
-                                o2[n][i].y += y;
-                            }
-                        }
-                    }
+            __syncwarp();
+            if (lane == 0) {
+                // this warp is done with the value stage; the last of the 8 refills it
+                __threadfence_block();
+                if ((atomicAdd(&s_vcnt[vst], 1) & 7) == 7) {
+                    __threadfence_block();
+                    const int y = s_y[(jt + p.nstage_v) % kYRing];
+                    if (y >= 0 && !*(volatile int*)&s_abort) issue_v(jt + p.nstage_v, y);
                 }
-                if (v_rg == 0) {
-#pragma unroll
-                    for (int n = 0; n < 4; ++n) {
-                        const int qi = ti.it.qs * QC + 4 * v_qg + n;
-                        if (qi < p.hpk * p.T) {
-                            const int t = qi / p.hpk, h = v_g * p.hpk + qi % p.hpk;
-                            const long long rec = (long long)ti.it.pidx * p.Qtot + (long long)t * p.Hq + h;
-#pragma unroll
-                            for (int cc = 0; cc < 4; ++cc) {
-                                const int dim = v_bi * 32 + 8 * v_hf + (cc & 1) * 4 + (cc >> 1) * 16;
-                                *reinterpret_cast<float4*>(&p.part_o[rec * D + dim]) =
-                                    make_float4(o2[n][2 * cc].x + pm[n], o2[n][2 * cc].y + pm[n],
-                                                o2[n][2 * cc + 1].x + pm[n], o2[n][2 * cc + 1].y + pm[n]);
-                            }
-                        }
-                    }
-                }
-                // (max, sum) of the softmax queries this warp owns
-#pragma unroll
-                for (int i = 0; i < NQMAX / 8; ++i) {
-                    const int qq = vw + 8 * i;
-                    if (qq < NQ) {
-                        float l = lsum[i];
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-                        const int g = qq / QC, ql = qq % QC;
-                        const int qi = ti.it.qs * QC + ql;
-                        if (lane == 0 && qi < p.hpk * p.T) {
-                            const int t = qi / p.hpk, h = g * p.hpk + qi % p.hpk;
-                            const long long rec = (long long)ti.it.pidx * p.Qtot + (long long)t * p.Hq + h;
-                            p.part_ml[rec * 2] = m_ref[i];
-                            p.part_ml[rec * 2 + 1] = l;
-                        }
-                        m_ref[i] = kNegInf;
-                        lsum[i] = 0.f;
-                    }
-                }
+            }
+            bar_arrive(BAR_EMPTY + slot, kKVThreads);      // and with the probabilities of tile jt
+            if (tinf.y) {
+                // row-group partial sums meet inside the warp: butterfly over
+                // the lane-group bits (TW is a power of two), one query at a
+                // time; lane group 0 writes the partial and every lane restarts
 #pragma unroll
                 for (int n = 0; n < 4; ++n) {
+                    for (int msk = TW; msk < 32; msk <<= 1) {
+                        pm[n] += __shfl_xor_sync(0xffffffffu, pm[n], msk);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            o2[n][i].x += __shfl_xor_sync(0xffffffffu, o2[n][i].x, msk);
+                            o2[n][i].y += __shfl_xor_sync(0xffffffffu, o2[n][i].y, msk);
+                        }
+                    }
+                    const int qi = t_qs * QC + 4 * v_qg + n;
+                    if (v_rg == 0 && qi < p.hpk * p.T) {
+                        int hr;
+                            const int t = qdiv(qi, p.hpk, inv_hpk, hr), h = v_g * p.hpk + hr;
+                        const long long rec = (long long)t_pidx * p.Qtot + (long long)t * p.Hq + h;
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const int dim = v_bi * 32 + 8 * v_hf + (cc & 1) * 4 + (cc >> 1) * 16;
+                            *reinterpret_cast<float4*>(&p.part_o[rec * D + dim]) =
+                                make_float4(o2[n][2 * cc].x + pm[n], o2[n][2 * cc].y + pm[n],
+                                            o2[n][2 * cc + 1].x + pm[n], o2[n][2 * cc + 1].y + pm[n]);
+                        }
+                    }
                     pm[n] = 0.f;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) o2[n][i] = make_float2(0.f, 0.f);
                 }
             }
-            advance(c, ti, p, lens, bases, prefix, n_items);
-            ++jt;
         }
+        if (tid == kKThreads && *(volatile int*)&s_abort)
+            for (int j = max(0, jt - p.nstage_v); j < jt; ++j) {
+                const long long t0 = clock64();
+                while (!mbar_try(smem_u32(&vfull[j % p.nstage_v]), (uint32_t)((j / p.nstage_v) & 1)) &&
+                       clock64() - t0 < kWaitCycles) {
+                }
+            }
     }
 }
 

@@ -19,7 +19,7 @@ constexpr int kMinSplitRows = 64;  // smallest rows-per-split the workspace allo
 constexpr int kMergeThreads = 1024;
 constexpr int kFastThreads = 512;  // warp-specialised decode CTA size
 constexpr int kFastRows = 32;      // rows per tile of the warp-specialised decode
-constexpr int kFastSDepth = 4;     // score buffers between its key and value warps
+constexpr int kFastPDepth = 4;     // probability buffers between its key and value warps
 
 // device error word codes
 constexpr int kErrCounter = 1;     // a length/base counter was out of range
@@ -72,11 +72,12 @@ struct SplitParams {
     int v_boxes;                   // 128-byte column blocks per value row
     int red_heads;                 // KV heads per round of the row-group reduction
     int nlimb;                     // int8 limbs per quantised query element (2 or 3)
+    int q_stage;                   // 1: stage the next item's queries in shared memory (cp.async)
 };
 
 // Shared-memory layout of the warp-specialised decode kernel (host and device).
 struct FastLayout {
-    size_t kstage, vstage, kring, vring, qlimb, qscale, S, P, alpha, mrun, lrun, red, lens, bars, total;
+    size_t kstage, vstage, kring, vring, qlimb, qscale, qraw, S, P, alpha, mrun, lrun, red, lens, bars, total;
 };
 
 __host__ __device__ inline size_t fl_round(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -99,12 +100,13 @@ __host__ __device__ inline FastLayout fast_layout(const SplitParams& p, int nlim
     off += fl_round(NQ * p.D * nlimb, 16);
     L.qscale = off;
     off += fl_round(NQ * NBH * 4, 16);
+    L.qraw = off;                  // next item's raw queries [NQ][D] (bf16 or f32)
+    off += p.q_stage ? fl_round(NQ * p.D * (p.q_bf16 ? 2 : 4), 16) : 0;
     L.S = off;
-    off += fl_round((size_t)kFastSDepth * NQ * kFastRows * 4, 16);
     L.P = off;
-    off += fl_round(2 * (size_t)kFastRows * (NQ + 4) * 4, 16);
+    off += fl_round((size_t)kFastPDepth * kFastRows * (NQ + 4) * 4, 16);
     L.alpha = off;
-    off += fl_round(2 * NQ * 4, 16);
+    off += fl_round((size_t)kFastPDepth * NQ * 4, 16);
     L.mrun = off;
     off += fl_round(NQ * 4, 16);
     L.lrun = off;
