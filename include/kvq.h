@@ -147,6 +147,28 @@ kvq_status kvq_decode(kvq_cache* cache, const void* q, kvq_dtype dtype, int T,
                       int n_q_heads, const float* sinks, float scale,
                       float* out, void* stream);
 
+/* Bytes of the no-alloc decode scratch (a fixed device array in the library). */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* kvq_decode without the cache's workspace: the described design has no
+ * counterpart of this call; it lets a caller decode without providing
+ * partial-result memory.  Same arguments, semantics and results as
+ * kvq_decode (the same kernels run on the same split plan), but the split
+ * partials and the plan live in a file-scope device array of
+ * KVQ_NOALLOC_SCRATCH_BYTES (16 MiB) inside the library: the call allocates
+ * nothing.  The decode needs n_seq * ceil(max visible rows / split rows) *
+ * n_q_heads * T * (head_dim + 2) * 4 bytes plus the plan; a call that needs
+ * more returns KVQ_ERANGE (nothing launched) and says how much.  Nothing in
+ * the array has to start at zero: every byte read was written earlier in the
+ * same call.  The first call on a device resolves the array's address
+ * (cudaGetSymbolAddress, with that device current): make it before any stream
+ * capture.  All calls share the one array per device, so two calls whose
+ * kernels may overlap (other streams, other threads, other caches) race:
+ * order them on one stream or synchronise between them. */
+kvq_status kvq_decode_noalloc(kvq_cache* cache, const void* q, kvq_dtype dtype, int T,
+                              int n_q_heads, const float* sinks, float scale,
+                              float* out, void* stream);
+
 /* Rollback ("Struct Cache", fn rollback, item C.1): set each sequence's
  * length to new_len[b] (a HOST array of n_seq values, usually
  * snapshot_len + accept_len), no data moves.  Needs new_len[b] <= len; a ring

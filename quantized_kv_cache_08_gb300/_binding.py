@@ -16,6 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libkvq.so")
 
 KVQ_OK, KVQ_EINVAL, KVQ_ERANGE, KVQ_ECUDA, KVQ_EUNSUPPORTED = 0, 1, 2, 3, 4
+KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 KVQ_F32, KVQ_BF16 = 0, 1
 KVQ_Q8_0, KVQ_Q5_1 = 0, 1
 
@@ -24,7 +25,7 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ERANGE", 3: "KVQ_ECUDA", 4
 # every symbol include/kvq.h declares
 EXPORTS = (
     "kvq_required_bytes", "kvq_alloc", "kvq_free", "kvq_append", "kvq_decode",
-    "kvq_truncate", "kvq_get_len", "kvq_note_replayed", "kvq_ring_headroom",
+    "kvq_decode_noalloc", "kvq_truncate", "kvq_get_len", "kvq_note_replayed", "kvq_ring_headroom",
     "kvq_physical_rows", "kvq_read_device_error", "kvq_set_split_rows", "kvq_set_decode_path",
     "kvq_block_bytes", "kvq_bytes_per_token", "kvq_last_error",
 )
@@ -69,6 +70,7 @@ def lib():
             "kvq_free": (None, [P]),
             "kvq_append": (I, [P, P, P, I, I, IP, I, P]),
             "kvq_decode": (I, [P, P, I, I, I, P, ctypes.c_float, P, P]),
+            "kvq_decode_noalloc": (I, [P, P, I, I, I, P, ctypes.c_float, P, P]),
             "kvq_truncate": (I, [P, IP, P]),
             "kvq_get_len": (I, [P, IP, IP]),
             "kvq_note_replayed": (I, [P, I, I]),
@@ -131,6 +133,10 @@ def kvq_append(handle, k, v, dtype, T, seq_ids=None, stream=0):
 
 def kvq_decode(handle, q, dtype, T, n_q_heads, sinks, scale, out, stream=0):
     _check(lib().kvq_decode(handle, q, dtype, T, n_q_heads, sinks, float(scale), out, stream))
+
+
+def kvq_decode_noalloc(handle, q, dtype, T, n_q_heads, sinks, scale, out, stream=0):
+    _check(lib().kvq_decode_noalloc(handle, q, dtype, T, n_q_heads, sinks, float(scale), out, stream))
 
 
 def kvq_truncate(handle, new_len, stream=0):

@@ -8,10 +8,13 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
 using namespace kvq;
+
+static constexpr int kMaxDevices = 64;
 
 struct kvq_cache {
     CUtensorMap kmap, vmap;              // 3-D TMA maps of the planes (warp-specialised decode)
@@ -292,8 +295,11 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, kvq_dtype dtyp
     return KVQ_OK;
 }
 
-kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n_q_heads, const float* sinks,
-                      float scale, float* out, void* stream) {
+// Decode through the cache's workspace (scratch == nullptr) or through the
+// caller-given scratch of scratch_bytes (partials, split plan).
+static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n_q_heads,
+                              const float* sinks, float scale, float* out, void* stream, unsigned char* scratch,
+                              size_t scratch_bytes) {
     if (!c) return fail(KVQ_EINVAL, "cache is NULL");
     if (!q || !out) return fail(KVQ_EINVAL, "q or out is NULL");
     if (dtype != KVQ_F32 && dtype != KVQ_BF16) return fail(KVQ_EINVAL, "dtype must be f32 or bf16");
@@ -355,9 +361,24 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
     p.QC = QC;
     p.nqs = (Q + QC - 1) / QC;
     p.Qtot = n_q_heads * T;
-    p.part_o = reinterpret_cast<float*>(c->ws + c->off_part_o);
-    p.part_ml = reinterpret_cast<float*>(c->ws + c->off_part_ml);
-    p.plan = reinterpret_cast<int*>(c->ws + c->off_plan);
+    if (scratch) {
+        // records: at most max_splits splits per sequence, whatever the
+        // device lengths are when the kernels run
+        const size_t recs = (size_t)B * max_splits * p.Qtot;
+        const size_t o_ml = round_up(recs * D * sizeof(float), 256);
+        const size_t o_plan = round_up(o_ml + recs * 2 * sizeof(float), 256);
+        const size_t need = o_plan + (B + 1) * sizeof(int);
+        if (need > scratch_bytes)
+            return fail(KVQ_ERANGE, "this decode needs %zu bytes of scratch, the no-alloc entry point holds %zu",
+                        need, scratch_bytes);
+        p.part_o = reinterpret_cast<float*>(scratch);
+        p.part_ml = reinterpret_cast<float*>(scratch + o_ml);
+        p.plan = reinterpret_cast<int*>(scratch + o_plan);
+    } else {
+        p.part_o = reinterpret_cast<float*>(c->ws + c->off_part_o);
+        p.part_ml = reinterpret_cast<float*>(c->ws + c->off_part_ml);
+        p.plan = reinterpret_cast<int*>(c->ws + c->off_plan);
+    }
     // a tile is staged as the 16-byte aligned superset of its rows' bytes
     p.k_stage_bytes = (uint32_t)round_up((size_t)kTileRows * c->k_tok + 32, 128);
     p.stage_bytes = p.k_stage_bytes + (uint32_t)round_up((size_t)kTileRows * c->v_tok + 32, 128);
@@ -415,6 +436,34 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
     e = launch_merge(m, T, max_splits, true, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode merge kernel");
     return KVQ_OK;
+}
+
+kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n_q_heads, const float* sinks,
+                      float scale, float* out, void* stream) {
+    return decode_impl(c, q, dtype, T, n_q_heads, sinks, scale, out, stream, nullptr, 0);
+}
+
+// Decode scratch of kvq_decode_noalloc: one file-scope device array per
+// device (the module's copy on each device), resolved once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+kvq_status kvq_decode_noalloc(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n_q_heads,
+                              const float* sinks, float scale, float* out, void* stream) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(KVQ_EUNSUPPORTED, "device %d beyond %d devices", dev, kMaxDevices);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!addr[dev]) {
+            e = cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the no-alloc scratch");
+        }
+    }
+    return decode_impl(c, q, dtype, T, n_q_heads, sinks, scale, out, stream,
+                       static_cast<unsigned char*>(addr[dev]), KVQ_NOALLOC_SCRATCH_BYTES);
 }
 
 kvq_status kvq_truncate(kvq_cache* c, const int* new_len, void* stream) {
