@@ -205,11 +205,12 @@ kvq_status kvq_read_device_error(kvq_cache* cache, int* err, void* stream);
  * is a power of two <= 128, and its tiles fit shared memory, else the generic
  * split kernel), 1 = generic, 2 = warp-specialised
  * (KVQ_EUNSUPPORTED at decode time if the geometry does not allow it).
- * query_bits (0 = 24, or 16): the warp-specialised kernel quantises each
- * pre-scaled query element per 32-element block to this many bits against
- * the block's largest magnitude and multiplies with int8 dot products; 24
- * bits is at the level of fp32 rounding, 16 bits adds an error below 1e-4
- * to the attention output on unit-variance data. */
+ * query_bits (0 = 16, or 16, or 24): the warp-specialised kernel quantises
+ * each pre-scaled query element per 32-element block to this many bits
+ * against the block's largest magnitude and multiplies with int8 dot
+ * products; 16 bits adds an error below 1e-4 to the attention output on
+ * unit-variance data, 24 bits is at the level of fp32 rounding and costs a
+ * third more dot products. */
 kvq_status kvq_set_decode_path(kvq_cache* cache, int path, int query_bits);
 
 /* Override the decode split size in rows (a multiple of 8, >= 64; 0 = auto). */

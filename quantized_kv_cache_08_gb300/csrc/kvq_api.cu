@@ -189,7 +189,7 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* 
                  make_row_tensor_map(&c->kmap, k_plane, g.k_tok, (long long)cfg->n_seq * g.rows) &&
                  make_row_tensor_map(&c->vmap, v_plane, g.v_tok, (long long)cfg->n_seq * g.rows);
     c->path = 0;
-    c->nlimb = 3;
+    c->nlimb = 2;                          // 16-bit queries unless 24 is asked for
     c->len.assign(cfg->n_seq, 0);
     c->base.assign(cfg->n_seq, 0);
     e = cudaMemsetAsync(counters, 0, counters_bytes(cfg->n_seq), static_cast<cudaStream_t>(stream));
@@ -554,7 +554,7 @@ kvq_status kvq_set_decode_path(kvq_cache* c, int path, int query_bits) {
     if (query_bits != 0 && query_bits != 16 && query_bits != 24)
         return fail(KVQ_EINVAL, "query_bits must be 0, 16 or 24");
     c->path = path;
-    c->nlimb = query_bits == 16 ? 2 : 3;
+    c->nlimb = query_bits == 24 ? 3 : 2;
     return KVQ_OK;
 }
 
