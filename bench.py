@@ -48,6 +48,23 @@ def kv_bytes_per_row(wl):
     return kb * (34 + 24)
 
 
+def decode_lengths(wl):
+    """Lengths at decode.  A ring holds the same visible rows at any length
+    past window + T, so its caches fill to twice the window instead of the
+    workload's final length (the decode then reads the same bytes)."""
+    lens = wl.lengths()
+    if wl.ring:
+        lens = [min(L, 2 * wl.window) for L in lens]
+    return lens
+
+
+def visible_rows(wl, L):
+    """Rows a T-row decode reads: the union of the query rows' windows."""
+    if wl.window:
+        return L - max(0, L - wl.T + 1 - wl.window)
+    return L
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -166,33 +183,52 @@ def run_kvq(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = workload(args.workload)
-    if wl.name not in ("ctx32k", "ctx512", "batch64"):
-        raise SystemExit("bench.py times the flat T=1 decode workloads (ctx32k, ctx512, batch64)")
-    lens = wl.lengths()
+    T = wl.T
+    lens = decode_lengths(wl)
     row_bytes = kv_bytes_per_row(wl)
-    footprint = sum(lens) * row_bytes
-    R = args.layers or max(1, math.ceil(3 * L2_BYTES / footprint))
-    T = 1
+    vis = [visible_rows(wl, L) for L in lens]
+    footprint = sum(vis) * row_bytes
+    R = args.layers or min(8, max(1, math.ceil(3 * L2_BYTES / footprint)))
+    flush = R * footprint < 3 * L2_BYTES
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
+    sinks = wl.sink_logits()
+    sinks_d = None if sinks is None else sinks.to(dev)
+    scratch = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
 
-    # --- build R layer caches holding len-1 rows each (prefill, untimed)
+    # --- build R layer caches holding len-T rows each (prefill, untimed);
+    # a ring fills with T-row steps, a flat cache with 64-row chunks
     caches = []
     for r in range(R):
-        c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=64, max_rows=max(lens))
+        if wl.ring:
+            c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=T, window=wl.window, ring=True)
+        else:
+            c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=64, max_rows=max(lens),
+                        window=wl.window)
+        chunk = T if wl.ring else 64
         for b, L in enumerate(lens):
-            k, v = wl.kv(b + 1000 * r + 100000 * rank, 0, L - 1)
+            k, v = wl.kv(b + 1000 * r + 100000 * rank, 0, L - T + 64 * T)
             kd, vd = k.to(dev), v.to(dev)
-            for t0 in range(0, L - 1, 64):
-                t1 = min(L - 1, t0 + 64)
+            for t0 in range(0, L - T, chunk):
+                t1 = min(L - T, t0 + chunk)
                 c.append(kd[t0:t1].unsqueeze(0), vd[t0:t1].unsqueeze(0), seq_ids=[b])
+            if wl.ring and r == 0:
+                # the step appends T rows and truncates them again: fill on
+                # until that append needs no rebase and the window of the
+                # truncated length is still resident, then every layer
+                # fills to that length
+                n = L - T
+                while c.ring_headroom(T) < 1 or n - T + 1 - wl.window < c.bases()[b]:
+                    c.append(kd[n:n + T].unsqueeze(0), vd[n:n + T].unsqueeze(0), seq_ids=[b])
+                    n += T
+                lens[b] = n + T
         caches.append(c)
-    base_len = [L - 1 for L in lens]
+    base_len = [L - T for L in lens]
     # --- per-layer step inputs, resident on the device
     k_new, v_new, qs = [], [], []
     for r in range(R):
-        kk = torch.stack([wl.kv(b + 1000 * r + 100000 * rank, L - 1, L)[0] for b, L in enumerate(lens)])
-        vv = torch.stack([wl.kv(b + 1000 * r + 100000 * rank, L - 1, L)[1] for b, L in enumerate(lens)])
+        kk = torch.stack([wl.kv(b + 1000 * r + 100000 * rank, L - T, L)[0] for b, L in enumerate(lens)])
+        vv = torch.stack([wl.kv(b + 1000 * r + 100000 * rank, L - T, L)[1] for b, L in enumerate(lens)])
         k_new.append(kk.to(dev))
         v_new.append(vv.to(dev))
         qs.append(wl.q(r + 7 * rank, T=T).to(dev))
@@ -201,11 +237,13 @@ def run_kvq(args, world, rank, local):
     torch.cuda.synchronize()
 
     def step(events=None):
+        if scratch is not None:
+            scratch.zero_()                 # inputs smaller than L2: flush it every step
         for r, c in enumerate(caches):
             c.append(k_new[r], v_new[r])
             if events is not None:
                 events[r][0].record(stream)
-            c.decode(qs[r], out=outs[r])
+            c.decode(qs[r], sinks=sinks_d, out=outs[r])
             if events is not None:
                 events[r][1].record(stream)
             c.truncate(base_len)
@@ -234,7 +272,7 @@ def run_kvq(args, world, rank, local):
     with torch.cuda.graph(g_dec, stream=stream):
         for k in range(args.steps):
             for r, c in enumerate(caches):
-                c.decode(qs[r], out=outs[r])
+                c.decode(qs[r], sinks=sinks_d, out=outs[r])
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         g_warm.replay()
@@ -273,10 +311,10 @@ def run_kvq(args, world, rank, local):
         if c.device_error() != 0:
             raise SystemExit("device error word set during the benchmark")
 
-    kv_bytes_step = R * sum(lens) * row_bytes           # per rank
+    kv_bytes_step = R * footprint                       # per rank
     decodes = args.steps * R
     value = world * kv_bytes_step * args.steps / (dec_ms * 1e-3) / 1e9
-    tokens_per_s = world * wl.n_seq * T * decodes / (dec_ms * 1e-3)
+    tokens_per_s = world * wl.n_seq * T * decodes / (dec_ms * 1e-3)   # query rows per second
     achieved = kv_bytes_step * args.steps / (dec_ms * 1e-3) / 1e9  # per GPU
     peak, peak_src = measured_peak()
 
@@ -295,7 +333,7 @@ def run_kvq(args, world, rank, local):
             dv[r].copy_(pin_v[r], non_blocking=True)
             dq[r].copy_(pin_q[r], non_blocking=True)
             c.append(dk[r], dv[r])
-            c.decode(dq[r], out=outs[r])
+            c.decode(dq[r], sinks=sinks_d, out=outs[r])
             pin_o[r].copy_(outs[r], non_blocking=True)
             c.truncate(base_len)
 
@@ -315,12 +353,20 @@ def run_kvq(args, world, rank, local):
     d2h = sum(x.numel() * x.element_size() for x in pin_o)
     e2e_value = world * kv_bytes_step * args.steps / (e2e_ms * 1e-3) / 1e9
 
+    extra = ""
+    if wl.window:
+        extra += f", window {wl.window}" + (f" over a ring of {caches[0].rows} rows" if wl.ring else "")
+    if sinks is not None:
+        extra += ", a sink logit per Q head"
     cfg = {"workload": f"{wl.name}: {wl.n_seq} seq, {wl.n_q} Q / {wl.n_kv} KV heads, head_dim "
-                       f"{wl.head_dim}, {sum(lens)} rows, T=1, q {wl.q_dtype}, K q8_0 / V q5_1",
-           "layers": R, "rows_total": sum(lens),
-           "kv_bytes_per_decode": sum(lens) * row_bytes,
-           "step": "per layer: append 1 row + decode + truncate back",
-           "l2": f"inputs larger than L2: {R} layer caches, {R * footprint / 1e6:.0f} MB rotated"}
+                       f"{wl.head_dim}, {sum(lens)} rows at decode, T={T}{extra}, q {wl.q_dtype}, "
+                       f"K q8_0 / V q5_1",
+           "layers": R, "rows_total": sum(lens), "rows_visible": sum(vis),
+           "kv_bytes_per_decode": footprint,
+           "step": f"per layer: append {T} row(s) + decode + truncate back",
+           "l2": (f"L2 flushed every step ({2 * L2_BYTES // 2**20} MiB write), {R} layer caches"
+                  if flush else
+                  f"inputs larger than L2: {R} layer caches, {R * footprint / 1e6:.0f} MB rotated")}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -341,11 +387,11 @@ def run_kvq(args, world, rank, local):
         "clocks": clk,
     }
     if rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(wl, lens)
+        line["cpu_baseline"] = cpu_baseline(wl, lens, sinks=sinks)
     return line
 
 
-def cpu_baseline(wl, lens, budget_s=12.0):
+def cpu_baseline(wl, lens, budget_s=12.0, sinks=None):
     """The fp64 oracle, as it stands, on a bounded sample of the workload: the
     decode of one layer for the first sequence (quantise its rows once, then
     dequantise + attend per repetition)."""
@@ -353,18 +399,19 @@ def cpu_baseline(wl, lens, budget_s=12.0):
 
     L = lens[0]
     k, v = wl.kv(0, 0, L)
-    ora = O.OracleKvCache(1, wl.n_kv, wl.head_dim)
+    ora = O.OracleKvCache(1, wl.n_kv, wl.head_dim, window=wl.window)
     ora.append(k.unsqueeze(0).numpy(), v.unsqueeze(0).numpy())
-    q = wl.q(0, T=1)[:1].float().numpy().astype("float64")
+    q = wl.q(0)[:1].float().numpy().astype("float64")
+    sk = None if sinks is None else sinks.double().numpy()
     reps, t_total = 0, 0.0
     while t_total < budget_s and reps < 20:
         t = time.perf_counter()
-        ora.decode(q)
+        ora.decode(q, sinks=sk)
         t_total += time.perf_counter() - t
         reps += 1
-    gbs = reps * L * kv_bytes_per_row(wl) / t_total / 1e9
+    gbs = reps * visible_rows(wl, L) * kv_bytes_per_row(wl) / t_total / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{reps} fp64 decodes of 1 sequence x {L} rows ({wl.name}), "
+            "sample": f"{reps} fp64 decodes of 1 sequence x {visible_rows(wl, L)} visible rows ({wl.name}), "
                       f"numpy with its default BLAS threading, {t_total:.1f} s"}
 
 
@@ -373,8 +420,9 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     wl = workload(args.workload)
-    lens = wl.lengths()
-    base = cpu_baseline(wl, lens, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    lens = decode_lengths(wl)
+    base = cpu_baseline(wl, lens, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)),
+                        sinks=wl.sink_logits())
     return {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
