@@ -9,7 +9,7 @@
 // column blocks, 128-byte swizzle) into its own ring of stages.  The last of
 // the 8 warps that read a stage (a shared-memory counter decides) issues the
 // copy that refills it, with the row coordinate from a small look-ahead table
-// that K warp 0 keeps filled, so no warp waits to issue copies.  Warps 0-7
+// that a value thread keeps filled, so no warp waits to issue copies.  Warps 0-7
 // (K warps) turn key rows into scores and run the online softmax; warps 8-15
 // (V warps) accumulate p * v_hat.  Probabilities
 // pass from K to V warps through a ring of kPDepth buffers handed over with
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
     __shared__ int4 s_tinfo[kPDepth];               // per probability buffer: rows, last, query slice, record (-1 rows: end)
     __shared__ int s_y[kYRing];                     // row coordinate of tile j in the planes' maps (-1: no tile j)
     __shared__ int s_kcnt[4], s_vcnt[4];            // releases per key / value stage (8 per use)
-    __shared__ Cursor s_ahead;                      // thread 0's look-ahead cursor
+    __shared__ int4 s_ahead;                        // the row table's cursor: next row, tiles left, item
 
     for (int b = tid; b < p.B; b += kThreads) {
         lens[b] = p.len_d[b];
@@ -366,7 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
         mbar_expect_tx(vfull_a + 8u * st, vstage_b);
         tma_load_rows(vring_a + st * vstage_b, vmap_p, y, vfull_a + 8u * st);
     };
-    const int LA = max(p.nstage_k, p.nstage_v);     // look-ahead of the row table
+    // look-ahead of the row table: V thread 0 fills it, and the V warps may
+    // trail the K warps by kPDepth + 1 tiles
+    const int LA = max(p.nstage_k, p.nstage_v) + kPDepth + 1;
 
     if (warp < 8) {
         // ======================================================== K warps
@@ -442,9 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                     }
                     if (jt == 0 && u0 == 0 && tid == 0) {
                         // the first query loads are out, ahead of the tile stream:
-                        // thread 0 starts a cursor LA tiles ahead (kept in shared
-                        // memory for the row table) and issues the first copies,
-                        // tile 0's key and value first
+                        // thread 0 fills the row table's first LA entries, leaves
+                        // its cursor in shared memory for the V thread that
+                        // continues it, and issues the first copies, tile 0's key
+                        // and value first
                         Cursor ahead = cursor_begin(p, lens, bases, prefix, n_items);
                         for (int j2 = 0; j2 < LA; ++j2) {
                             int y = -1;
@@ -457,7 +460,14 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                             if (y >= 0 && j2 < p.nstage_k) issue_k(j2, y);
                             if (y >= 0 && j2 < p.nstage_v) issue_v(j2, y);
                         }
-                        s_ahead = ahead;
+                        // hand the cursor over as (next row, tiles left, item)
+                        int4 a = make_int4(0, 0, ahead.item, 0);
+                        if (ahead.item < n_items) {
+                            const TileInfo ta = tile_of(ahead);
+                            a.x = ta.b * p.max_rows + (ta.r0 - ta.base);
+                            a.y = (ahead.n - ahead.tile * kRows + kRows - 1) / kRows;
+                        }
+                        s_ahead = a;
                     }
 #pragma unroll
                     for (int j = 0; j < QB; ++j) {
@@ -526,18 +536,6 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                     }
                     asm volatile("cp.async.commit_group;" ::: "memory");
                 }
-            }
-            if (tid == 0) {
-                // row coordinate of tile jt + LA, before this warp's release below
-                Cursor ahead = s_ahead;
-                int y = -1;
-                if (ahead.item < n_items) {
-                    const TileInfo ta = tile_of(ahead);
-                    y = ta.b * p.max_rows + (ta.r0 - ta.base);
-                    advance(ahead, ta, p, lens, bases, prefix, n_items);
-                }
-                s_y[(jt + LA) % kYRing] = y;
-                s_ahead = ahead;
             }
             // ------------------------------------------------ scores
             const int kst = jt % p.nstage_k;
@@ -689,6 +687,31 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
             bar_sync(BAR_FULL + slot, kKVThreads);         // probabilities of tile jt are in
             const int4 tinf = s_tinfo[slot];
             if (tinf.x < 0) break;                         // the K warps' end mark
+            if (tid == kKThreads) {
+                // row coordinate of tile jt + LA for the copy refills (the
+                // barrier above orders it before the releases that read it):
+                // next row, tiles left in its item; an item is decoded only
+                // when the cursor enters it
+                int4 a = s_ahead;                          // y, tiles left, item, -
+                int y = -1;
+                if (a.z < n_items) {
+                    y = a.x;
+                    if (a.y > 1) {
+                        a.x += kRows;
+                        a.y -= 1;
+                    } else {
+                        a.z += (int)gridDim.x;
+                        if (a.z < n_items) {
+                            const Item it = item_of(a.z, prefix, p.B, p.nqs);
+                            const ItemRows ir = item_rows(p, lens, bases, it);
+                            a.x = it.b * p.max_rows + (ir.row0 - ir.base);
+                            a.y = (ir.n + kRows - 1) / kRows;
+                        }
+                    }
+                }
+                s_y[(jt + LA) % kYRing] = y;
+                s_ahead = a;
+            }
             const int t_nr = tinf.x, t_qs = tinf.z, t_pidx = tinf.w;
             const float* Pb = P + slot * kRows * PS;
             const float* ab = alpha + slot * NQ;
