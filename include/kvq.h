@@ -95,7 +95,7 @@ typedef struct kvq_config {
  *             128 bytes of padding (tile copies move whole 128-byte column
  *             blocks), rounded up to a multiple of 256 bytes
  *   v_plane   [n_seq][max_rows][kb*24]  (padded and rounded likewise)
- *   counters  len_d[n_seq], base_d[n_seq], error word (int32)
+ *   counters  len_d[n_seq], base_d[n_seq], error word, work-item counter (int32)
  *   workspace decode partials, the split plan and the ring-rebase scratch   */
 typedef struct kvq_sizes {
     size_t k_plane, v_plane, counters, workspace;

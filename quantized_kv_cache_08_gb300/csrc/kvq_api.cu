@@ -25,6 +25,7 @@ struct kvq_cache {
     int* len_d;
     int* base_d;
     int* err_d;
+    int* work_d;                         // decode work-item counter (0 between decodes)
     uint8_t* ws;
     size_t off_part_o, off_part_ml, off_plan, off_scratch;
     int kb, k_tok, v_tok, rows;          // rows = physical rows per sequence
@@ -108,7 +109,7 @@ WsLayout ws_layout(const kvq_config* c, const Geometry& g) {
     return w;
 }
 
-size_t counters_bytes(int n_seq) { return round_up((2 * (size_t)n_seq + 1) * sizeof(int), 256); }
+size_t counters_bytes(int n_seq) { return round_up((2 * (size_t)n_seq + 2) * sizeof(int), 256); }
 
 // visible-row start of a T-row step
 int vis_lo(const kvq_cache* c, int len, int T) {
@@ -172,6 +173,7 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* 
     c->len_d = static_cast<int*>(counters);
     c->base_d = c->len_d + cfg->n_seq;
     c->err_d = c->base_d + cfg->n_seq;
+    c->work_d = c->err_d + 1;
     c->ws = static_cast<uint8_t*>(workspace);
     const WsLayout w = ws_layout(cfg, g);
     c->off_part_o = w.part_o;
@@ -327,12 +329,15 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         if (c->len[b] < T) return fail(KVQ_ERANGE, "sequence %d holds %d rows, fewer than T=%d", b, c->len[b], T);
         total_vis += c->len[b] - vis_lo(c, c->len[b], T);
     }
-    // rows per split: one wave of items for one sequence, ~16 items per CTA otherwise
+    // rows per split: one wave of items for one sequence; otherwise about 5
+    // items per CTA in whole 32-row tiles (an item start costs a query
+    // preparation, a partial last tile costs nearly a full one; CTAs take
+    // items dynamically, so the tail costs about half an item)
     int C = c->split_rows;
     if (C == 0) {
         const long long per = B == 1 ? (total_vis + c->num_sms - 1) / c->num_sms
-                                     : (total_vis + 16LL * c->num_sms - 1) / (16LL * c->num_sms);
-        C = (int)std::max<long long>(kMinSplitRows, round_up((size_t)per, 8));
+                                     : (total_vis + 5LL * c->num_sms - 1) / (5LL * c->num_sms);
+        C = (int)std::max<long long>(kMinSplitRows, round_up((size_t)per, B == 1 ? 8 : 32));
     }
     const int max_splits = (c->max_vis + C - 1) / C;
 
@@ -343,6 +348,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     p.len_d = c->len_d;
     p.base_d = c->base_d;
     p.err_d = c->err_d;
+    p.work_d = c->work_d;
     p.q = q;
     p.q_bf16 = dtype == KVQ_BF16;
     p.qscale = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
@@ -428,6 +434,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     m.part_ml = p.part_ml;
     m.plan = p.plan;
     m.sinks = sinks;
+    m.work_d = c->work_d;
     m.out = out;
     m.B = B;
     m.Hq = n_q_heads;

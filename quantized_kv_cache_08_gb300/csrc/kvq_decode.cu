@@ -476,9 +476,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitPara
 // largest merge CTA for VPL values per lane (registers: U splits of VPL in flight)
 __host__ __device__ constexpr int merge_threads(int vpl) { return vpl <= 2 ? kMergeThreads : vpl <= 8 ? 512 : 256; }
 
-template <int VPL>
+template <int VPL, int U>
 __global__ void __launch_bounds__(merge_threads(VPL)) merge_kernel(const MergeParams p, int QPB, int SW) {
-    constexpr int U = VPL >= 8 ? 4 : 8;             // splits whose loads are in flight together
+    // U: splits whose loads are in flight together in a warp
     extern __shared__ float msm[];                  // [QPB][SW][2 + D]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qi = warp % QPB, sg = warp / QPB;
@@ -486,6 +486,8 @@ __global__ void __launch_bounds__(merge_threads(VPL)) merge_kernel(const MergePa
     const int b = blockIdx.y;
     const int D = VPL * 32;
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the split grid has completed: its work-item counter restarts at 0
+    if (p.work_d && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.work_d = 0;
     const bool live = gq < p.Qtot;
     const int first = p.plan[b];
     const int ns = live ? p.plan[b + 1] - first : 0;
@@ -610,7 +612,7 @@ cudaError_t launch_split(const SplitParams& p, int grid, cudaStream_t s) {
     return cudaErrorInvalidValue;
 }
 
-template <int VPL>
+template <int VPL, int U>
 cudaError_t launch_merge_t(const MergeParams& p, int max_splits, bool pdl, cudaStream_t s) {
     // split warps per query: enough that each folds about four splits, up
     // to a whole CTA; queries per CTA fill the remaining warps
@@ -620,7 +622,7 @@ cudaError_t launch_merge_t(const MergeParams& p, int max_splits, bool pdl, cudaS
     int QPB = 1;
     while (QPB * 2 * SW <= NW && QPB * 2 <= p.Qtot) QPB *= 2;
     const size_t smem = (size_t)QPB * SW * (2 + VPL * 32) * sizeof(float);
-    auto fn = merge_kernel<VPL>;
+    auto fn = merge_kernel<VPL, U>;
     // same shared-memory carveout as the split kernels, so merge CTAs launched
     // early (programmatic dependent launch) can wait beside the split CTAs
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -644,12 +646,16 @@ cudaError_t launch_merge_t(const MergeParams& p, int max_splits, bool pdl, cudaS
 
 cudaError_t launch_merge(const MergeParams& p, int T, int max_splits, bool pdl, cudaStream_t s) {
     (void)T;
+    // twice the loads in flight when one warp folds more than 8 splits, so
+    // every split's record is requested in the first round (head_dim 128 or
+    // 256; smaller heads run 32 warps a CTA)
+    const bool deep = max_splits > 8 * (merge_threads(p.D / 32) / 32);
     switch (p.D / 32) {
-        case 1: return launch_merge_t<1>(p, max_splits, pdl, s);
-        case 2: return launch_merge_t<2>(p, max_splits, pdl, s);
-        case 4: return launch_merge_t<4>(p, max_splits, pdl, s);
-        case 8: return launch_merge_t<8>(p, max_splits, pdl, s);
-        case 16: return launch_merge_t<16>(p, max_splits, pdl, s);
+        case 1: return launch_merge_t<1, 8>(p, max_splits, pdl, s);    // 32 warps: 256 splits a round
+        case 2: return launch_merge_t<2, 8>(p, max_splits, pdl, s);
+        case 4: return deep ? launch_merge_t<4, 16>(p, max_splits, pdl, s) : launch_merge_t<4, 8>(p, max_splits, pdl, s);
+        case 8: return deep ? launch_merge_t<8, 8>(p, max_splits, pdl, s) : launch_merge_t<8, 4>(p, max_splits, pdl, s);
+        case 16: return launch_merge_t<16, 4>(p, max_splits, pdl, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -118,10 +118,22 @@ __device__ __forceinline__ void wait_stage(uint32_t bar, uint32_t parity, volati
 // Tile cursor over this CTA's items (blockIdx.x, +gridDim.x, ...), with the
 // current item's decode cached so a tile step costs no division.
 struct Cursor {
-    int item, tile;
+    int item, tile, k;             // k: the item's ordinal among this CTA's items
     Item it;
     int row0, n, base, len;
 };
+
+// Work items: a CTA's first item is blockIdx.x; later ones come from a
+// device counter, so CTAs that finish early take more.  The copy look-ahead
+// reserves item k + 1 of the CTA when it enters item k and publishes the
+// CTA's item order in a small shared-memory queue that the K warps follow.
+constexpr int kIRing = 16;
+
+__device__ __forceinline__ int reserve_item(int* work_d, int n_items) {
+    if (n_items <= (int)gridDim.x) return n_items;     // every item is in the first wave
+    const int nx = (int)gridDim.x + atomicAdd(work_d, 1);
+    return nx < n_items ? nx : n_items;
+}
 
 struct TileInfo {
     int b, r0, nr, base, len;
@@ -145,6 +157,7 @@ __device__ __forceinline__ Cursor cursor_begin(const SplitParams& p, const int* 
     Cursor c;
     c.item = blockIdx.x;
     c.tile = 0;
+    c.k = 0;
     cursor_load(c, p, lens, bases, prefix, n_items);
     return c;
 }
@@ -163,9 +176,10 @@ __device__ __forceinline__ TileInfo tile_of(const Cursor& c) {
 }
 
 __device__ __forceinline__ void advance(Cursor& c, const TileInfo& ti, const SplitParams& p, const int* lens,
-                                        const int* bases, const int* prefix, int n_items) {
+                                        const int* bases, const int* prefix, int n_items, const int* items) {
     if (ti.last) {
-        c.item += gridDim.x;
+        ++c.k;
+        c.item = items[c.k % kIRing];
         c.tile = 0;
         cursor_load(c, p, lens, bases, prefix, n_items);
     } else {
@@ -326,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
     __shared__ int4 s_tinfo[kPDepth];               // per probability buffer: rows, last, query slice, record (-1 rows: end)
     __shared__ int s_y[kYRing];                     // row coordinate of tile j in the planes' maps (-1: no tile j)
     __shared__ int s_kcnt[4], s_vcnt[4];            // releases per key / value stage (8 per use)
-    __shared__ int4 s_ahead;                        // the row table's cursor: next row, tiles left, item
+    __shared__ int4 s_ahead;                        // the row table's cursor: next row, tiles left, item, ordinal
+    __shared__ int s_items[kIRing];                 // item of this CTA's k-th work item (n_items: none)
 
     for (int b = tid; b < p.B; b += kThreads) {
         lens[b] = p.len_d[b];
@@ -448,20 +463,36 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                         // its cursor in shared memory for the V thread that
                         // continues it, and issues the first copies, tile 0's key
                         // and value first
+                        // (item 1 is reserved after the first copies are out,
+                        // or when the walk reaches the end of item 0)
+                        s_items[0] = blockIdx.x;
+                        bool have1 = false;
                         Cursor ahead = cursor_begin(p, lens, bases, prefix, n_items);
                         for (int j2 = 0; j2 < LA; ++j2) {
                             int y = -1;
-                            if (ahead.item < n_items) {
-                                const TileInfo ta = tile_of(ahead);
+                            const bool live = ahead.item < n_items;
+                            TileInfo ta;
+                            if (live) {
+                                ta = tile_of(ahead);
                                 y = ta.b * p.max_rows + (ta.r0 - ta.base);
-                                advance(ahead, ta, p, lens, bases, prefix, n_items);
                             }
                             s_y[j2] = y;
                             if (y >= 0 && j2 < p.nstage_k) issue_k(j2, y);
                             if (y >= 0 && j2 < p.nstage_v) issue_v(j2, y);
+                            if (live) {
+                                if (ta.last && ahead.k == 0) {
+                                    s_items[1] = reserve_item(p.work_d, n_items);
+                                    have1 = true;
+                                }
+                                const int k0 = ahead.k;
+                                advance(ahead, ta, p, lens, bases, prefix, n_items, s_items);
+                                if (ahead.k != k0 && ahead.item < n_items)
+                                    s_items[(ahead.k + 1) % kIRing] = reserve_item(p.work_d, n_items);
+                            }
                         }
+                        if (!have1) s_items[1] = reserve_item(p.work_d, n_items);
                         // hand the cursor over as (next row, tiles left, item)
-                        int4 a = make_int4(0, 0, ahead.item, 0);
+                        int4 a = make_int4(0, 0, ahead.item, ahead.k);
                         if (ahead.item < n_items) {
                             const TileInfo ta = tile_of(ahead);
                             a.x = ta.b * p.max_rows + (ta.r0 - ta.base);
@@ -516,10 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                     qlo[qq] = p.window > 0 ? max(0, upto - p.window) : 0;
                 }
                 bar_sync(BAR_K, kKThreads);          // limbs and row windows visible to every K warp
-                if (p.q_stage && c.item + (int)gridDim.x < n_items) {
+                const int nx_item = s_items[(c.k + 1) % kIRing];
+                if (p.q_stage && nx_item < n_items) {
                     // stage the next item's raw queries: 16-byte cp.async
                     // chunks of each query row (rows of absent queries skipped)
-                    const Item nx = item_of(c.item + (int)gridDim.x, prefix, p.B, p.nqs);
+                    const Item nx = item_of(nx_item, prefix, p.B, p.nqs);
                     const int esz = p.q_bf16 ? 2 : 4;
                     const int cpr = D * esz / 16;    // chunks per query row
                     for (int ch = kt; ch < NQ * cpr; ch += kKThreads) {
@@ -635,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                     }
                 }
             }
-            advance(c, ti, p, lens, bases, prefix, n_items);
+            advance(c, ti, p, lens, bases, prefix, n_items, s_items);
             ++jt;
         }
         // copies still landing after a wait ran out must finish before the CTA ends
@@ -681,6 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
             for (int i = 0; i < 8; ++i) o2[n][i] = make_float2(0.f, 0.f);
         }
         int jt = 0;
+        int pend_k = -1, pend_item = 0;                 // look-ahead thread: reservation not yet published
 #pragma unroll 1
         for (;; ++jt) {
             const int slot = jt % kPDepth;
@@ -691,8 +724,14 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                 // row coordinate of tile jt + LA for the copy refills (the
                 // barrier above orders it before the releases that read it):
                 // next row, tiles left in its item; an item is decoded only
-                // when the cursor enters it
-                int4 a = s_ahead;                          // y, tiles left, item, -
+                // when the cursor enters it.  The item reserved on entering
+                // an item is published one step later, off the atomic's
+                // round trip.
+                int4 a = s_ahead;                          // y, tiles left, item, ordinal
+                if (pend_k >= 0) {
+                    s_items[pend_k % kIRing] = pend_item;
+                    pend_k = -1;
+                }
                 int y = -1;
                 if (a.z < n_items) {
                     y = a.x;
@@ -700,8 +739,11 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                         a.x += kRows;
                         a.y -= 1;
                     } else {
-                        a.z += (int)gridDim.x;
+                        a.w += 1;
+                        a.z = s_items[a.w % kIRing];
                         if (a.z < n_items) {
+                            pend_item = reserve_item(p.work_d, n_items);
+                            pend_k = a.w + 1;
                             const Item it = item_of(a.z, prefix, p.B, p.nqs);
                             const ItemRows ir = item_rows(p, lens, bases, it);
                             a.x = it.b * p.max_rows + (ir.row0 - ir.base);

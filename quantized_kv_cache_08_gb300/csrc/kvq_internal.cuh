@@ -51,6 +51,7 @@ struct SplitParams {
     const int* len_d;
     const int* base_d;
     int* err_d;
+    int* work_d;                   // work items handed out past the first wave (reset by the merge)
     const void* q;                 // [B][T][Hq][D]
     int q_bf16;
     float qscale;                  // score scale * log2(e)
@@ -126,6 +127,7 @@ struct MergeParams {
     const float* part_ml;
     const int* plan;               // [B+1]
     const float* sinks;            // [Hq] or null
+    int* work_d;                   // the split kernel's work-item counter, reset here
     float* out;                    // [B][T][Hq][D]
     int B, Hq, Qtot, D;
 };
