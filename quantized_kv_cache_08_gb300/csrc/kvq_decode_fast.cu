@@ -49,7 +49,8 @@ constexpr int kPDepth = kFastPDepth;           // probability buffers between K 
 constexpr int kKThreads = 256;                 // warps 0-7
 constexpr int kKVThreads = 512;                // K and V warps
 constexpr int kYRing = 16;                     // look-ahead table of tile row coordinates
-constexpr int BAR_K = 1, BAR_FULL = 2, BAR_EMPTY = 2 + kPDepth;
+constexpr int BAR_K = 1, BAR_FULL = 2, BAR_EMPTY = 2 + kPDepth, BAR_QLOAD = 2 + 2 * kPDepth,
+              BAR_INIT = 3 + 2 * kPDepth;
 constexpr long long kWaitCycles = 1LL << 31;   // ~1 s bound on any mbarrier wait
 
 __device__ __forceinline__ void bar_sync(int id, int n) {
@@ -457,49 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                             }
                         }
                     }
-                    if (jt == 0 && u0 == 0 && tid == 0) {
-                        // the first query loads are out, ahead of the tile stream:
-                        // thread 0 fills the row table's first LA entries, leaves
-                        // its cursor in shared memory for the V thread that
-                        // continues it, and issues the first copies, tile 0's key
-                        // and value first
-                        // (item 1 is reserved after the first copies are out,
-                        // or when the walk reaches the end of item 0)
-                        s_items[0] = blockIdx.x;
-                        bool have1 = false;
-                        Cursor ahead = cursor_begin(p, lens, bases, prefix, n_items);
-                        for (int j2 = 0; j2 < LA; ++j2) {
-                            int y = -1;
-                            const bool live = ahead.item < n_items;
-                            TileInfo ta;
-                            if (live) {
-                                ta = tile_of(ahead);
-                                y = ta.b * p.max_rows + (ta.r0 - ta.base);
-                            }
-                            s_y[j2] = y;
-                            if (y >= 0 && j2 < p.nstage_k) issue_k(j2, y);
-                            if (y >= 0 && j2 < p.nstage_v) issue_v(j2, y);
-                            if (live) {
-                                if (ta.last && ahead.k == 0) {
-                                    s_items[1] = reserve_item(p.work_d, n_items);
-                                    have1 = true;
-                                }
-                                const int k0 = ahead.k;
-                                advance(ahead, ta, p, lens, bases, prefix, n_items, s_items);
-                                if (ahead.k != k0 && ahead.item < n_items)
-                                    s_items[(ahead.k + 1) % kIRing] = reserve_item(p.work_d, n_items);
-                            }
-                        }
-                        if (!have1) s_items[1] = reserve_item(p.work_d, n_items);
-                        // hand the cursor over as (next row, tiles left, item)
-                        int4 a = make_int4(0, 0, ahead.item, ahead.k);
-                        if (ahead.item < n_items) {
-                            const TileInfo ta = tile_of(ahead);
-                            a.x = ta.b * p.max_rows + (ta.r0 - ta.base);
-                            a.y = (ahead.n - ahead.tile * kRows + kRows - 1) / kRows;
-                        }
-                        s_ahead = a;
-                    }
+                    // the first query loads are out, ahead of the tile stream:
+                    // the value thread that starts the copies may go
+                    if (jt == 0 && u0 == 0) bar_arrive(BAR_QLOAD, kKThreads + 32);
 #pragma unroll
                     for (int j = 0; j < QB; ++j) {
                         const int u = u0 + j * kKThreads + kt;
@@ -547,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                     qlo[qq] = p.window > 0 ? max(0, upto - p.window) : 0;
                 }
                 bar_sync(BAR_K, kKThreads);          // limbs and row windows visible to every K warp
+                if (jt == 0) bar_sync(BAR_INIT, kKThreads + 32);   // the first copies and item 1 are set
                 const int nx_item = s_items[(c.k + 1) % kIRing];
                 if (p.q_stage && nx_item < n_items) {
                     // stage the next item's raw queries: 16-byte cp.async
@@ -711,6 +673,53 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
             pm[n] = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) o2[n][i] = make_float2(0.f, 0.f);
+        }
+        if (vw == 0) {
+            bar_sync(BAR_QLOAD, kKThreads + 32);
+            if (lane == 0) {
+                // the first query loads are out, ahead of the tile stream:
+                // this thread fills the row table's first LA entries,
+                // issues the first copies (tile 0's key and value first),
+                // reserves item 1 after them (or when the walk reaches the
+                // end of item 0) and keeps its cursor in shared memory for
+                // the per-tile look-ahead below
+                s_items[0] = blockIdx.x;
+                bool have1 = false;
+                Cursor ahead = cursor_begin(p, lens, bases, prefix, n_items);
+                for (int j2 = 0; j2 < LA; ++j2) {
+                    int y = -1;
+                    const bool live = ahead.item < n_items;
+                    TileInfo ta;
+                    if (live) {
+                        ta = tile_of(ahead);
+                        y = ta.b * p.max_rows + (ta.r0 - ta.base);
+                    }
+                    s_y[j2] = y;
+                    if (y >= 0 && j2 < p.nstage_k) issue_k(j2, y);
+                    if (y >= 0 && j2 < p.nstage_v) issue_v(j2, y);
+                    if (live) {
+                        if (ta.last && ahead.k == 0) {
+                            s_items[1] = reserve_item(p.work_d, n_items);
+                            have1 = true;
+                        }
+                        const int k0 = ahead.k;
+                        advance(ahead, ta, p, lens, bases, prefix, n_items, s_items);
+                        if (ahead.k != k0 && ahead.item < n_items)
+                            s_items[(ahead.k + 1) % kIRing] = reserve_item(p.work_d, n_items);
+                    }
+                }
+                if (!have1) s_items[1] = reserve_item(p.work_d, n_items);
+                // hand the cursor over as (next row, tiles left, item)
+                int4 a = make_int4(0, 0, ahead.item, ahead.k);
+                if (ahead.item < n_items) {
+                    const TileInfo ta = tile_of(ahead);
+                    a.x = ta.b * p.max_rows + (ta.r0 - ta.base);
+                    a.y = (ahead.n - ahead.tile * kRows + kRows - 1) / kRows;
+                }
+                s_ahead = a;
+            }
+            __syncwarp();
+            bar_arrive(BAR_INIT, kKThreads + 32);
         }
         int jt = 0;
         int pend_k = -1, pend_item = 0;                 // look-ahead thread: reservation not yet published
