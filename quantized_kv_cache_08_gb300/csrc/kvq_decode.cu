@@ -524,17 +524,24 @@ __global__ void __launch_bounds__(merge_threads(VPL)) merge_kernel(const MergePa
                 o4[u][0] = ok ? src[0] : 0.f;
             }
         }
+        // the round's maximum first, then independent weights: one rescale
+        // of the running state per round instead of a chain per split
+        float Mr = M;
+#pragma unroll
+        for (int u = 0; u < U; ++u) Mr = fmaxf(Mr, m4[u]);
+        if (Mr == kNegInf) continue;                // nothing visible in this round
+        const float a = (M == kNegInf) ? 0.f : exp2f(M - Mr);
+        L *= a;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) acc[v] *= a;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            if (m4[u] == kNegInf) continue;
-            const float Mn = fmaxf(M, m4[u]);
-            const float a = (M == kNegInf) ? 0.f : exp2f(M - Mn);
-            const float w = exp2f(m4[u] - Mn);
-            L = L * a + l4[u] * w;
+            const float w = (m4[u] == kNegInf) ? 0.f : exp2f(m4[u] - Mr);
+            L = fmaf(l4[u], w, L);
 #pragma unroll
-            for (int v = 0; v < VPL; ++v) acc[v] = acc[v] * a + o4[u][v] * w;
-            M = Mn;
+            for (int v = 0; v < VPL; ++v) acc[v] = fmaf(o4[u][v], w, acc[v]);
         }
+        M = Mr;
     }
     float* st = msm + (size_t)(qi * SW + sg) * (2 + D);
     if (lane == 0) {
@@ -549,11 +556,13 @@ __global__ void __launch_bounds__(merge_threads(VPL)) merge_kernel(const MergePa
         const float sink = p.sinks ? p.sinks[gq % p.Hq] * LOG2E : kNegInf;
         const float* q0 = msm + (size_t)qi * SW * (2 + D);
         float Mt = sink;
+#pragma unroll 8
         for (int w = 0; w < SW; ++w) Mt = fmaxf(Mt, q0[w * (2 + D)]);
         float Lt = (sink == kNegInf) ? 0.f : exp2f(sink - Mt);
         float At[VPL];
 #pragma unroll
         for (int v = 0; v < VPL; ++v) At[v] = 0.f;
+#pragma unroll 4
         for (int w = 0; w < SW; ++w) {
             const float* e = q0 + w * (2 + D);
             if (e[0] == kNegInf) continue;
