@@ -99,6 +99,16 @@ __device__ __forceinline__ int qdiv(int a, int b, float inv_b, int& rem) {
     return q;
 }
 
+// One warp's release of a stage: an acquire-release add on the stage's
+// shared-memory counter, so the warp's reads of the stage happen before a
+// refill that the last releaser issues.
+__device__ __forceinline__ uint32_t release_count(int* counter) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                 : "=r"(old) : "r"(smem_u32(counter)) : "memory");
+    return old;
+}
+
 // Bounded wait that gives up for the whole CTA once any wait has run out: the
 // error word is set, later waits return at once, and every thread still runs
 // the full barrier protocol (results are then garbage but the kernel ends).
@@ -553,9 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
             __syncwarp();
             if (lane == 0) {
                 // this warp is done with the key stage; the last of the 8 refills it
-                __threadfence_block();
-                if ((atomicAdd(&s_kcnt[kst], 1) & 7) == 7) {
-                    __threadfence_block();
+                if ((release_count(&s_kcnt[kst]) & 7) == 7) {
                     const int y = s_y[(jt + p.nstage_k) % kYRing];
                     if (y >= 0 && !*(volatile int*)&s_abort) issue_k(jt + p.nstage_k, y);
                 }
@@ -850,9 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
             __syncwarp();
             if (lane == 0) {
                 // this warp is done with the value stage; the last of the 8 refills it
-                __threadfence_block();
-                if ((atomicAdd(&s_vcnt[vst], 1) & 7) == 7) {
-                    __threadfence_block();
+                if ((release_count(&s_vcnt[vst]) & 7) == 7) {
                     const int y = s_y[(jt + p.nstage_v) % kYRing];
                     if (y >= 0 && !*(volatile int*)&s_abort) issue_v(jt + p.nstage_v, y);
                 }
