@@ -400,7 +400,6 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     if (fast) {
         bool fits = false;
         const int depths[4][2] = {{3, 3}, {3, 2}, {2, 3}, {2, 2}};
-        p.red_heads = 1;
         // stage next-item queries in shared memory when there is room and the
         // query rows are 16-byte aligned
         for (int stage_q = ((uintptr_t)q % 16 == 0) ? 1 : 0; stage_q >= 0 && !fits; --stage_q) {

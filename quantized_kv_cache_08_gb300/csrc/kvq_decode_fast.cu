@@ -1,20 +1,25 @@
 // Warp-specialised split-K decode for caches whose token rows are 16-byte
-// multiples (n_kv_heads * head_dim % 256 == 0).  Same semantics, work items,
-// partial records and merge as the generic split kernel (kvq_decode.cu):
+// multiples (n_kv_heads * head_dim % 256 == 0).  Same semantics, partial
+// records and merge as the generic split kernel (kvq_decode.cu):
 // cortiq-engine "Struct LayerKvCache" fn attend_group_upto (window, causal
 // upto, sinks, GQA) over memra-engine "Struct KvLayer" q8_0 / q5_1 rows.
+//
+// Persistent CTAs, one per SM.  A CTA's first work item is its block index;
+// later items come from a device counter (the merge resets it), so CTAs that
+// finish early take more.
 //
 // A CTA has 16 warps.  The key and the value bytes of a 32-row tile each
 // arrive by one 3-D TMA copy (cp.async.bulk.tensor, 32 rows x all 128-byte
 // column blocks, 128-byte swizzle) into its own ring of stages.  The last of
-// the 8 warps that read a stage (a shared-memory counter decides) issues the
-// copy that refills it, with the row coordinate from a small look-ahead table
-// that a value thread keeps filled, so no warp waits to issue copies.  Warps 0-7
-// (K warps) turn key rows into scores and run the online softmax; warps 8-15
-// (V warps) accumulate p * v_hat.  Probabilities
-// pass from K to V warps through a ring of kPDepth buffers handed over with
-// named barriers (bar.arrive / bar.sync), so the K warps may run up to
-// kPDepth tiles ahead.
+// the 8 warps that read a stage (an acquire-release shared counter decides)
+// issues the copy that refills it, with the row coordinate from a small
+// look-ahead table that one value thread keeps filled; that thread also
+// reserves the CTA's next work item and publishes the CTA's item order, which
+// the key warps follow.  No warp waits to issue copies.  Warps 0-7 (K warps)
+// turn key rows into scores and run the online softmax; warps 8-15 (V warps)
+// accumulate p * v_hat.  Probabilities pass from K to V warps through a ring
+// of kPDepth buffers handed over with named barriers (bar.arrive / bar.sync),
+// so the K warps may run up to kPDepth tiles ahead.
 //
 // K warps: lane = token row; a warp owns whole (KV head, query group of 4)
 // units.  The swizzle puts the same 16-byte column of 8 consecutive rows in 8
@@ -22,9 +27,11 @@
 // 16-byte loads.  The query is pre-scaled by scale * log2 e, quantised per
 // (query, 32-element block) to NLIMB*8 bits against the block's largest
 // magnitude and split into int8 limbs held in shared memory; every lane reads
-// the same limb words (broadcast).  DP4A multiplies four int8 codes by four
-// limb bytes and accumulates in int32, so the codes are never converted to
-// float; per block the limb sums are combined in float and scaled by d_k * s_q.
+// the same limb words (broadcast).  The next item's raw queries are staged in
+// shared memory (cp.async) while the current item runs.  DP4A multiplies four
+// int8 codes by four limb bytes and accumulates in int32, so the codes are
+// never converted to float; per block the limb sums are combined in float and
+// scaled by d_k * s_q.
 // Softmax: the unit's scores of a tile sit one row per lane, so the reference
 // maximum is a warp reduction.  It moves only when a score exceeds it by more
 // than 8 (log2 units); a warp vote finds that rare case, otherwise
@@ -340,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
     uint8_t* qraw = smem + L.qraw;
     float* P = reinterpret_cast<float*>(smem + L.P);            // [kPDepth][kRows][PS]
     float* alpha = reinterpret_cast<float*>(smem + L.alpha);    // [kPDepth][NQ]
-    int* qlo = reinterpret_cast<int*>(smem + L.mrun);           // [NQ] first visible row per CTA query
-    int* qup = reinterpret_cast<int*>(smem + L.lrun);           // [NQ] one past the last (-1: no query)
+    int* qlo = reinterpret_cast<int*>(smem + L.qlo);            // [NQ] first visible row per CTA query
+    int* qup = reinterpret_cast<int*>(smem + L.qup);            // [NQ] one past the last (-1: no query)
     int* lens = reinterpret_cast<int*>(smem + L.lens);
     int* bases = lens + p.B;
     int* prefix = bases + p.B;

@@ -71,14 +71,13 @@ struct SplitParams {
     uint32_t k_row_stride;         // (generic layout only) stride of a staged key row
     int k_boxes;                   // 128-byte column blocks per key row
     int v_boxes;                   // 128-byte column blocks per value row
-    int red_heads;                 // KV heads per round of the row-group reduction
     int nlimb;                     // int8 limbs per quantised query element (2 or 3)
     int q_stage;                   // 1: stage the next item's queries in shared memory (cp.async)
 };
 
 // Shared-memory layout of the warp-specialised decode kernel (host and device).
 struct FastLayout {
-    size_t kstage, vstage, kring, vring, qlimb, qscale, qraw, S, P, alpha, mrun, lrun, red, lens, bars, total;
+    size_t kstage, vstage, kring, vring, qlimb, qscale, qraw, P, alpha, qlo, qup, lens, bars, total;
 };
 
 __host__ __device__ inline size_t fl_round(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -87,8 +86,6 @@ __host__ __device__ inline FastLayout fast_layout(const SplitParams& p, int nlim
     FastLayout L;
     const size_t NQ = (size_t)p.Hkv * p.QC;
     const size_t NBH = (size_t)p.D / 32;
-    const size_t nV = 2 * (size_t)(p.QC / 4) * p.Hkv * NBH;
-    const size_t rpV = nV ? 256 / nV : 1;
     // key tiles: k_boxes swizzled boxes of kFastRows x 128 bytes (1024-byte aligned)
     L.kstage = (size_t)p.k_boxes * kFastRows * 128;
     L.vstage = (size_t)p.v_boxes * kFastRows * 128;
@@ -103,17 +100,14 @@ __host__ __device__ inline FastLayout fast_layout(const SplitParams& p, int nlim
     off += fl_round(NQ * NBH * 4, 16);
     L.qraw = off;                  // next item's raw queries [NQ][D] (bf16 or f32)
     off += p.q_stage ? fl_round(NQ * p.D * (p.q_bf16 ? 2 : 4), 16) : 0;
-    L.S = off;
     L.P = off;
     off += fl_round((size_t)kFastPDepth * kFastRows * (NQ + 4) * 4, 16);
     L.alpha = off;
     off += fl_round((size_t)kFastPDepth * NQ * 4, 16);
-    L.mrun = off;
+    L.qlo = off;
     off += fl_round(NQ * 4, 16);
-    L.lrun = off;
+    L.qup = off;
     off += fl_round(NQ * 4, 16);
-    L.red = off;
-    (void)rpV;
     L.lens = off;
     off += fl_round((3 * (size_t)p.B + 1) * 4, 16);
     L.bars = off;
