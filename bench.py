@@ -5,8 +5,9 @@ exceed L2 several times): append one token's K/V (q8_0 / q5_1 quantise +
 commit), decode attention of one query row over the whole cache (split +
 merge kernels), and truncate the appended row again (rollback to
 snapshot_len + 0), so every step sees the same length.  Inputs are resident in
-HBM before the timed region; decode launches are bracketed by CUDA events on
-the launching stream to time the dominant kernel pair.
+HBM before the timed region.  The decode time is what the decode adds to the
+step: the captured K-step graph minus the same graph without the decodes, both
+timed by CUDA events around the replay on the launching stream.
 
 `value` is GB/s of quantised KV read by the decode (algorithmic bytes: every
 visible row x (K 34 + V 24 bytes per 32 elements)), summed over all ranks.
@@ -236,43 +237,60 @@ def run_kvq(args, world, rank, local):
             for _ in range(R)]
     torch.cuda.synchronize()
 
-    def step(events=None):
+    def step(events=None, decode=True):
         if scratch is not None:
             scratch.zero_()                 # inputs smaller than L2: flush it every step
         for r, c in enumerate(caches):
             c.append(k_new[r], v_new[r])
             if events is not None:
                 events[r][0].record(stream)
-            c.decode(qs[r], sinks=sinks_d, out=outs[r])
+            if decode:
+                c.decode(qs[r], sinks=sinks_d, out=outs[r])
             if events is not None:
                 events[r][1].record(stream)
             c.truncate(base_len)
 
-    # eager warm-up (kernel attributes, lazy module loads), then capture: one
-    # step for the untimed warm-up replays, K steps with event nodes around
-    # every decode for the timed replay.  The counters live on the device, so
-    # the captured append / decode / truncate replay with the right lengths.
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    def replay_ms(g):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    # eager warm-up (kernel attributes, lazy module loads), then capture.  The
+    # counters live on the device, so the captured append / decode / truncate
+    # replay with the right lengths.  The decode time is what the decode adds
+    # to the step: the K-step graph (the timed region) minus the same graph
+    # without the decodes, both timed by CUDA events around the replay on the
+    # launching stream.  Event nodes inside a graph cost microseconds each,
+    # so the per-decode event brackets and a graph of back-to-back decodes are
+    # reported beside it as cross-checks only.
     step()
     torch.cuda.synchronize()
-    g_warm = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_warm, stream=stream):
-        step()
+    g_warm = capture(step)
+    g_timed = capture(lambda: [step() for _ in range(args.steps)])
+    g_nodec = capture(lambda: [step(decode=False) for _ in range(args.steps)])
     try:   # event record nodes inside the graph (torch >= 2.6 'external' events)
         ev = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
                for _ in range(R)] for _ in range(args.steps)]
+        g_ev = capture(lambda: [step(ev[k]) for k in range(args.steps)])
     except TypeError:
-        ev = None
-    g_timed = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_timed, stream=stream):
-        for k in range(args.steps):
-            step(None if ev is None else ev[k])
-    # decode-only graph: the fallback timing of the decode when in-graph
-    # events are unavailable, and a cross-check of it otherwise
-    g_dec = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_dec, stream=stream):
-        for k in range(args.steps):
+        ev, g_ev = None, None
+
+    def dec_only():
+        for _ in range(args.steps):
             for r, c in enumerate(caches):
                 c.decode(qs[r], sinks=sinks_d, out=outs[r])
+    g_dec = capture(dec_only)
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         g_warm.replay()
@@ -281,32 +299,21 @@ def run_kvq(args, world, rank, local):
     clocks = Clocks(local)
     clocks.start()
     time.sleep(0.3)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    t0.record(stream)
-    g_timed.replay()
-    t1.record(stream)
-    torch.cuda.synchronize()
+    step_ms = statistics.median(replay_ms(g_timed) for _ in range(3))
     clk = clocks.stop()
     barrier(world)
-    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
-    d0 = torch.cuda.Event(enable_timing=True)
-    d1 = torch.cuda.Event(enable_timing=True)
+    nodec_ms = statistics.median(replay_ms(g_nodec) for _ in range(3))
     g_dec.replay()
-    torch.cuda.synchronize()
-    d0.record(stream)
-    g_dec.replay()
-    d1.record(stream)
-    torch.cuda.synchronize()
-    dec_only_ms = max_over_ranks(d0.elapsed_time(d1), world)
-    if ev is not None:
-        dec_ms = sum(a.elapsed_time(b) for evk in ev for a, b in evk)
-        timing = "CUDA graph of K steps, event nodes around each decode"
-    else:
-        dec_ms = dec_only_ms
-        timing = "CUDA graph of K steps; decode timed in a graph of K x R back-to-back decodes"
-    dec_ms = max_over_ranks(dec_ms, world)
+    dec_only_ms = max_over_ranks(replay_ms(g_dec), world)
+    bracket_ms = None
+    if g_ev is not None:
+        g_ev.replay()
+        torch.cuda.synchronize()
+        bracket_ms = max_over_ranks(sum(a.elapsed_time(b) for evk in ev for a, b in evk), world)
+    total_ms = max_over_ranks(step_ms, world)
+    dec_ms = max_over_ranks(step_ms - nodec_ms, world)
+    timing = ("decode = CUDA-graph replay of K steps minus the same K steps without the decode, "
+              "CUDA events around each replay on the launching stream")
     for c in caches:
         if c.device_error() != 0:
             raise SystemExit("device error word set during the benchmark")
@@ -384,6 +391,8 @@ def run_kvq(args, world, rank, local):
         "gpu_launches": 5 * R * args.steps,
         "timing": timing,
         "decode_only_ms_per_layer": round(dec_only_ms / decodes, 5),
+        "decode_event_bracket_ms_per_layer": None if bracket_ms is None else round(bracket_ms / decodes, 5),
+        "step_without_decode_ms_per_layer": round(nodec_ms / decodes, 5),
         "clocks": clk,
     }
     if rank == 0 and world == 1:
