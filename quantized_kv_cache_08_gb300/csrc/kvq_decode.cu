@@ -580,7 +580,8 @@ __global__ void __launch_bounds__(merge_threads(VPL)) merge_kernel(const MergePa
 template <int NBH, int NQG>
 cudaError_t launch_split_t(const SplitParams& p, int grid, size_t smem, cudaStream_t s) {
     auto fn = split_kernel<NBH, NQG>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<unsigned long long> attrs{0};
+    cudaError_t e = kernel_attrs_once(fn, attrs, false);
     if (e != cudaSuccess) return e;
     fn<<<grid, kSplitThreads, smem, s>>>(p);
     return cudaGetLastError();
@@ -634,9 +635,8 @@ cudaError_t launch_merge_t(const MergeParams& p, int max_splits, bool pdl, cudaS
     auto fn = merge_kernel<VPL, U>;
     // same shared-memory carveout as the split kernels, so merge CTAs launched
     // early (programmatic dependent launch) can wait beside the split CTAs
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<unsigned long long> attrs{0};
+    cudaError_t e = kernel_attrs_once(fn, attrs, true);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((p.Qtot + QPB - 1) / QPB), (unsigned)p.B, 1);

@@ -918,7 +918,8 @@ template <int NBH, int NQG, int NLIMB>
 cudaError_t launch_t(const SplitParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid, size_t smem,
                      cudaStream_t s) {
     auto fn = fast_kernel<NBH, NQG, NLIMB>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<unsigned long long> attrs{0};
+    cudaError_t e = kernel_attrs_once(fn, attrs, false);
     if (e != cudaSuccess) return e;
     fn<<<grid, kThreads, smem, s>>>(p, kmap, vmap);
     return cudaGetLastError();

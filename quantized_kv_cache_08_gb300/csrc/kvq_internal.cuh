@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 namespace kvq {
 
 constexpr int kQK = 32;            // elements per quantisation block
@@ -81,6 +83,33 @@ struct FastLayout {
 };
 
 __host__ __device__ inline size_t fl_round(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Raise a kernel's dynamic shared-memory limit to the device's opt-in maximum
+// less its static shared memory (and, when carveout is set, prefer the
+// largest shared-memory carveout) once per device: `done` holds one bit per
+// device for that kernel.
+template <typename F>
+inline cudaError_t kernel_attrs_once(F fn, std::atomic<unsigned long long>& done, bool carveout) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    int smem = 0;
+    e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fn);              // the kernel's static shared memory counts too
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem - (int)fa.sharedSizeBytes);
+    if (e != cudaSuccess) return e;
+    if (carveout) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+    }
+    done.fetch_or(bit, std::memory_order_acq_rel);
+    return cudaSuccess;
+}
 
 __host__ __device__ inline FastLayout fast_layout(const SplitParams& p, int nlimb) {
     FastLayout L;
