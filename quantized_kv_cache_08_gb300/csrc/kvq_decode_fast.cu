@@ -429,91 +429,115 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const SplitParams p, 
                 if (staged) asm volatile("cp.async.wait_all;" ::: "memory");
                 bar_sync(BAR_K, kKThreads);          // previous item's scores are done; staged queries in
                 const int nunits = NQ * (D / 4);
-                constexpr int QB = 4;                // units per thread whose loads are in flight together
-                for (int u0 = 0; u0 < nunits; u0 += QB * kKThreads) {
-                    float xs[QB][4];
+                // one unit = 4 consecutive dims of a query: scale, block maximum
+                // over the unit's 8 lanes, int8 limbs and the block's scale
+                auto quant_unit = [&](const float (&xs4)[4], int u, bool act) {
+                    const int qq = act ? u / (D / 4) : 0, w4 = act ? u % (D / 4) : 0;
+                    const int bi = w4 >> 3, k = w4 & 7;
+                    const int g = qq / QC, ql = qq % QC;
+                    float x[4];
 #pragma unroll
-                    for (int j = 0; j < QB; ++j) {
-                        const int u = u0 + j * kKThreads + kt;
-                        const int qq = u / (D / 4), w4 = u % (D / 4);
-                        const int g = qq / QC, ql = qq % QC;
-                        const int qi = ti.it.qs * QC + ql;
+                    for (int e = 0; e < 4; ++e) x[e] = xs4[e] * p.qscale;
+                    // the 8 threads of a 32-dim block (consecutive lanes) share its maximum
+                    float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) xs[j][e] = 0.f;
-                        if (u < nunits && qi < p.hpk * p.T && staged) {
-                            if (p.q_bf16) {
-                                const uint2 raw = *reinterpret_cast<const uint2*>(qraw + ((size_t)qq * D + 4 * w4) * 2);
-                                xs[j][0] = __uint_as_float(raw.x << 16);
-                                xs[j][1] = __uint_as_float(raw.x & 0xffff0000u);
-                                xs[j][2] = __uint_as_float(raw.y << 16);
-                                xs[j][3] = __uint_as_float(raw.y & 0xffff0000u);
-                            } else {
-                                const float4 f = *reinterpret_cast<const float4*>(qraw + ((size_t)qq * D + 4 * w4) * 4);
-                                xs[j][0] = f.x;
-                                xs[j][1] = f.y;
-                                xs[j][2] = f.z;
-                                xs[j][3] = f.w;
-                            }
-                        } else if (u < nunits && qi < p.hpk * p.T) {
-                            int hr;
-                            const int t = qdiv(qi, p.hpk, inv_hpk, hr), h = g * p.hpk + hr;
-                            const long long base = ((long long)(ti.b * p.T + t) * p.Hq + h) * D + 4 * w4;
-                            if (p.q_bf16) {
-                                const uint2 raw = *reinterpret_cast<const uint2*>(
-                                    reinterpret_cast<const __nv_bfloat16*>(p.q) + base);
-                                xs[j][0] = __uint_as_float(raw.x << 16);
-                                xs[j][1] = __uint_as_float(raw.x & 0xffff0000u);
-                                xs[j][2] = __uint_as_float(raw.y << 16);
-                                xs[j][3] = __uint_as_float(raw.y & 0xffff0000u);
-                            } else {
-                                const float4 f =
-                                    *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.q) + base);
-                                xs[j][0] = f.x;
-                                xs[j][1] = f.y;
-                                xs[j][2] = f.z;
-                                xs[j][3] = f.w;
-                            }
-                        }
+                    for (int o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    constexpr float QMAX = NLIMB == 3 ? 8388607.f : 32767.f;
+                    // any scale works here: the dot products are rescaled by mx / QMAX
+                    const float inv = mx > 0.f ? __fdividef(QMAX, mx) : 0.f;
+                    int v4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int v = __float2int_rn(x[e] * inv);
+                        v4[e] = max(-(int)QMAX, min((int)QMAX, v));
                     }
-                    // the first query loads are out, ahead of the tile stream:
-                    // the value thread that starts the copies may go
-                    if (jt == 0 && u0 == 0) bar_arrive(BAR_QLOAD, kKThreads + 32);
+                    if (act) {
+                        const int qg = ql >> 2, n = ql & 3;
+                        const int unit = g * NQG + qg;
+                        uint32_t* dst = qlimb + (size_t)((unit * NBH + bi) * 8 + k) * NLIMB * 4;
 #pragma unroll
-                    for (int j = 0; j < QB; ++j) {
-                        const int u = u0 + j * kKThreads + kt;
-                        const bool act = u < nunits;
-                        const int qq = act ? u / (D / 4) : 0, w4 = act ? u % (D / 4) : 0;
-                        const int bi = w4 >> 3, k = w4 & 7;
-                        const int g = qq / QC, ql = qq % QC;
-                        float x[4];
+                        for (int l = 0; l < NLIMB; ++l) {
+                            uint32_t word = 0;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) x[e] = xs[j][e] * p.qscale;
-                        // the 8 threads of a 32-dim block (consecutive lanes) share its maximum
-                        float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-                        for (int o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                        constexpr float QMAX = NLIMB == 3 ? 8388607.f : 32767.f;
-                        // any scale works here: the dot products are rescaled by mx / QMAX
-                        const float inv = mx > 0.f ? __fdividef(QMAX, mx) : 0.f;
-                        int v4[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int v = __float2int_rn(x[e] * inv);
-                            v4[e] = max(-(int)QMAX, min((int)QMAX, v));
+                            for (int e = 0; e < 4; ++e) word |= (uint32_t)((v4[e] >> (8 * l)) & 0xff) << (8 * e);
+                            dst[l * 4 + n] = word;
                         }
-                        if (act) {
-                            const int qg = ql >> 2, n = ql & 3;
-                            const int unit = g * NQG + qg;
-                            uint32_t* dst = qlimb + (size_t)((unit * NBH + bi) * 8 + k) * NLIMB * 4;
+                        if (k == 0) qscl[(unit * NBH + bi) * 4 + n] = mx * (1.f / QMAX);
+                    }
+                };
+                constexpr int QB = 4;                // units per thread whose loads are in flight together
+                if (staged) {
+                    // queries already in shared memory (staged during the item before)
+                    for (int u0 = 0; u0 < nunits; u0 += QB * kKThreads) {
+                        float xs[QB][4];
 #pragma unroll
-                            for (int l = 0; l < NLIMB; ++l) {
-                                uint32_t word = 0;
+                        for (int j = 0; j < QB; ++j) {
+                            const int u = u0 + j * kKThreads + kt;
+                            const int qq = u / (D / 4), w4 = u % (D / 4);
+                            const int qi = ti.it.qs * QC + qq % QC;
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) word |= (uint32_t)((v4[e] >> (8 * l)) & 0xff) << (8 * e);
-                                dst[l * 4 + n] = word;
+                            for (int e = 0; e < 4; ++e) xs[j][e] = 0.f;
+                            if (u < nunits && qi < p.hpk * p.T) {
+                                if (p.q_bf16) {
+                                    const uint2 raw =
+                                        *reinterpret_cast<const uint2*>(qraw + ((size_t)qq * D + 4 * w4) * 2);
+                                    xs[j][0] = __uint_as_float(raw.x << 16);
+                                    xs[j][1] = __uint_as_float(raw.x & 0xffff0000u);
+                                    xs[j][2] = __uint_as_float(raw.y << 16);
+                                    xs[j][3] = __uint_as_float(raw.y & 0xffff0000u);
+                                } else {
+                                    const float4 f =
+                                        *reinterpret_cast<const float4*>(qraw + ((size_t)qq * D + 4 * w4) * 4);
+                                    xs[j][0] = f.x;
+                                    xs[j][1] = f.y;
+                                    xs[j][2] = f.z;
+                                    xs[j][3] = f.w;
+                                }
                             }
-                            if (k == 0) qscl[(unit * NBH + bi) * 4 + n] = mx * (1.f / QMAX);
                         }
+#pragma unroll
+                        for (int j = 0; j < QB; ++j)
+                            quant_unit(xs[j], u0 + j * kKThreads + kt, u0 + j * kKThreads + kt < nunits);
+                    }
+                } else {
+                    // the CTA's first item (or staging off): queries from global memory
+                    for (int u0 = 0; u0 < nunits; u0 += QB * kKThreads) {
+                        float xs[QB][4];
+#pragma unroll
+                        for (int j = 0; j < QB; ++j) {
+                            const int u = u0 + j * kKThreads + kt;
+                            const int qq = u / (D / 4), w4 = u % (D / 4);
+                            const int g = qq / QC, ql = qq % QC;
+                            const int qi = ti.it.qs * QC + ql;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) xs[j][e] = 0.f;
+                            if (u < nunits && qi < p.hpk * p.T) {
+                                int hr;
+                                const int t = qdiv(qi, p.hpk, inv_hpk, hr), h = g * p.hpk + hr;
+                                const long long base = ((long long)(ti.b * p.T + t) * p.Hq + h) * D + 4 * w4;
+                                if (p.q_bf16) {
+                                    const uint2 raw = *reinterpret_cast<const uint2*>(
+                                        reinterpret_cast<const __nv_bfloat16*>(p.q) + base);
+                                    xs[j][0] = __uint_as_float(raw.x << 16);
+                                    xs[j][1] = __uint_as_float(raw.x & 0xffff0000u);
+                                    xs[j][2] = __uint_as_float(raw.y << 16);
+                                    xs[j][3] = __uint_as_float(raw.y & 0xffff0000u);
+                                } else {
+                                    const float4 f =
+                                        *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.q) + base);
+                                    xs[j][0] = f.x;
+                                    xs[j][1] = f.y;
+                                    xs[j][2] = f.z;
+                                    xs[j][3] = f.w;
+                                }
+                            }
+                        }
+                        // the first query loads are out, ahead of the tile stream:
+                        // the value thread that starts the copies may go
+                        if (jt == 0 && u0 == 0) bar_arrive(BAR_QLOAD, kKThreads + 32);
+#pragma unroll
+                        for (int j = 0; j < QB; ++j)
+                            quant_unit(xs[j], u0 + j * kKThreads + kt, u0 + j * kKThreads + kt < nunits);
                     }
                 }
                 for (int qq = kt; qq < NQ; qq += kKThreads) {
