@@ -268,7 +268,7 @@ def dequantize_v_rows(rows, n_kv, head_dim) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 def attend(q, k_hat, v_hat, *, scale=None, sinks=None, window=0,
-           heads=None, rows_t=None):
+           heads=None, rows_t=None, softcap=0.0):
     """Decode attention of the last T rows of one sequence.
 
     q      [T, Hq, D]  (any float dtype; taken exactly as float64)
@@ -280,6 +280,10 @@ def attend(q, k_hat, v_hat, *, scale=None, sinks=None, window=0,
     Head h reads KV group h // (Hq // Hkv).  Scores are scale * <q, k_hat>,
     scale = 1/sqrt(D) when None.  A sink logit (per Q head, not scaled) joins
     the max and the denominator and carries no value.
+    softcap > 0 caps every scaled score s to softcap * tanh(s / softcap) before
+    the softmax (the pages pass a softcap to fn attend_group / attend_group_upto
+    without defining it; this is the usual logit soft-capping); the sink logit
+    is not capped.
     `heads` / `rows_t` restrict the computation to a subset (others are nan).
     Returns float64 [T, Hq, D]."""
     q = np.asarray(q, dtype=np.float64)
@@ -302,6 +306,8 @@ def attend(q, k_hat, v_hat, *, scale=None, sinks=None, window=0,
             kk = k_hat[lstart:upto, g, :]
             vv = v_hat[lstart:upto, g, :]
             s = scale * (kk @ q[t, h])
+            if softcap > 0:
+                s = softcap * np.tanh(s / softcap)
             sink = -math.inf if sinks is None else float(sinks[h])
             mx = max(sink, float(np.max(s)))
             w = np.exp(s - mx)
@@ -366,7 +372,7 @@ class OracleKvCache:
         return self._k[b][lo:hi], self._v[b][lo:hi]
 
     def decode(self, q, *, scale=None, sinks=None, heads=None, rows_t=None,
-               seqs=None):
+               seqs=None, softcap=0.0):
         """q [B, T, Hq, D] -> float64 [B, T, Hq, D] (nan where not computed)."""
         q = np.asarray(q, dtype=np.float64)
         out = np.full(q.shape, np.nan)
@@ -381,5 +387,6 @@ class OracleKvCache:
             # rows before `lo` have probability exactly 0 for every query row,
             # so attending the suffix with the same window is the same result
             out[b] = attend(q[b], kh, vh, scale=scale, sinks=sinks,
-                            window=self.window, heads=heads, rows_t=rows_t)
+                            window=self.window, heads=heads, rows_t=rows_t,
+                            softcap=softcap)
         return out

@@ -294,6 +294,39 @@ def test_ring_growth_matches_flat_oracle_and_keeps_invariants(path):
     assert_close(got, ref)
 
 
+@pytest.mark.parametrize("path", [1, 2])
+def test_ring_multi_row_chunks_match_windowed_oracle(path):
+    """Prefill-style chunks on the ring: T-row appends (T drawn from 1..16, the
+    ring sized window + 30 + max_t) each followed by the causal T-row decode;
+    live rows equal the oracle's logical rows and every step's outputs match
+    the windowed oracle, across many rebases."""
+    Hq, Hkv, D, W, MT, N = 16, 4, 64, 256, 16, 1500
+    p = Pair(1, Hkv, D, Hq, max_t=MT, window=W, ring=True)
+    p.dev.set_decode_path(path)
+    assert p.dev.rows == W + 30 + MT
+    k = _randn(1, N, Hkv, D, seed=111)
+    v = _randn(1, N, Hkv, D, seed=112)
+    s = _randn(Hq, seed=113)
+    rng = np.random.default_rng(114)
+    L, step = 0, 0
+    while True:
+        T = int(rng.integers(1, MT + 1))
+        if L + T > N:
+            break
+        p.append(k[:, L:L + T], v[:, L:L + T])
+        L += T
+        base = p.dev.bases()[0]
+        lstart = max(0, L - T + 1 - W)              # the first query row's window start
+        assert base <= lstart and L - base <= p.dev.rows
+        got, ref = p.decode(_randn(1, T, Hq, D, seed=2000 + step), sinks=s)
+        assert_close(got, ref, what=f"chunk {step} (T={T}, len {L})")
+        if step % 5 == 0:
+            assert_rows_equal(p.dev, p.ora, 0, lstart, L)
+        step += 1
+    assert step > 100 and p.dev.bases()[0] > 0
+    assert p.dev.device_error() == 0
+
+
 def test_flat_capacity_errors_enqueue_nothing():
     c = KVCache(1, 2, 64, 4, max_t=4, max_rows=6)
     x = torch.zeros(1, 4, 2, 64, device="cuda")

@@ -347,6 +347,35 @@ def test_attention_invariants():
     assert not np.allclose(wrong, plain)
 
 
+def test_softcap_limits_and_saturation():
+    """Score soft-capping (the softcap argument of cortiq-engine "Struct
+    LayerKvCache" fn attend_group / attend_group_upto, read as the usual
+    s -> c * tanh(s / c) on the scaled score, sink not capped), pinned by
+    limits and a closed form rather than by restating it."""
+    rng = np.random.default_rng(21)
+    L, Hq, Hkv, D = 24, 4, 2, 32
+    kh = rng.standard_normal((L, Hkv, D))
+    vh = rng.standard_normal((L, Hkv, D))
+    q = rng.standard_normal((1, Hq, D))
+    plain = O.attend(q, kh, vh)
+    # a cap far above every score changes nothing (a missing "c *" or "/ c"
+    # would make it uniform or explode)
+    np.testing.assert_allclose(O.attend(q, kh, vh, softcap=1e9), plain, rtol=0, atol=1e-12)
+    # softcap 0 is off
+    np.testing.assert_array_equal(O.attend(q, kh, vh, softcap=0.0), plain)
+    # saturation: huge scores cap to +-c exactly, so the weights are e^{+-c}
+    # by sign of q.k alone; the sink (not capped) joins with e^{sink}
+    c, sink = 1.5, 2.0
+    qb = q * 1e6
+    out = O.attend(qb, kh, vh, softcap=c, sinks=np.full(Hq, sink))
+    hpk = Hq // Hkv
+    for h in range(Hq):
+        sgn = np.sign(kh[:, h // hpk, :] @ qb[0, h])
+        w = np.exp(c * sgn)
+        want = (w @ vh[:, h // hpk, :]) / (np.exp(sink) + w.sum())
+        np.testing.assert_allclose(out[0, h], want, rtol=1e-12, atol=1e-12)
+
+
 def test_causal_rows_equal_sequential_append_then_attend():
     rng = np.random.default_rng(13)
     B, Hq, Hkv, D, T = 2, 8, 2, 64, 6
