@@ -213,6 +213,16 @@ kvq_status kvq_read_device_error(kvq_cache* cache, int* err, void* stream);
  * third more dot products. */
 kvq_status kvq_set_decode_path(kvq_cache* cache, int path, int query_bits);
 
+/* Score soft-capping for later decodes ("Struct LayerKvCache": the softcap
+ * argument of fn attend_group / attend_group_upto, which the pages name
+ * without defining; read as the usual logit soft-capping).  softcap > 0 maps
+ * every scaled score s = scale * <q, k_hat> to softcap * tanh(s / softcap)
+ * before the softmax; sink logits are not capped.  0 (the default) turns it
+ * off.  While a cap is set, decodes run the generic split kernel (a decode
+ * forced onto the warp-specialised kernel with kvq_set_decode_path path 2
+ * returns KVQ_EUNSUPPORTED).  KVQ_EINVAL for a negative or non-finite value. */
+kvq_status kvq_set_softcap(kvq_cache* cache, float softcap);
+
 /* Override the decode split size in rows (a multiple of 8, >= 64; 0 = auto). */
 kvq_status kvq_set_split_rows(kvq_cache* cache, int rows);
 

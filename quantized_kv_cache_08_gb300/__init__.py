@@ -11,5 +11,6 @@ from ._binding import (  # noqa: F401
     EXPORTS, KVQ_BF16, KVQ_F32, KVQ_Q5_1, KVQ_Q8_0, KvqError, kvq_alloc, kvq_append,
     kvq_block_bytes, kvq_bytes_per_token, kvq_decode, kvq_decode_noalloc, kvq_free, kvq_get_len, kvq_last_error,
     kvq_note_replayed, kvq_physical_rows, kvq_read_device_error, kvq_required_bytes,
-    kvq_ring_headroom, kvq_set_decode_path, kvq_set_split_rows, kvq_truncate, lib, make_config,
+    kvq_ring_headroom, kvq_set_decode_path, kvq_set_softcap, kvq_set_split_rows, kvq_truncate, lib,
+    make_config,
 )

@@ -27,6 +27,7 @@ EXPORTS = (
     "kvq_required_bytes", "kvq_alloc", "kvq_free", "kvq_append", "kvq_decode",
     "kvq_decode_noalloc", "kvq_truncate", "kvq_get_len", "kvq_note_replayed", "kvq_ring_headroom",
     "kvq_physical_rows", "kvq_read_device_error", "kvq_set_split_rows", "kvq_set_decode_path",
+    "kvq_set_softcap",
     "kvq_block_bytes", "kvq_bytes_per_token", "kvq_last_error",
 )
 
@@ -79,6 +80,7 @@ def lib():
             "kvq_read_device_error": (I, [P, IP, P]),
             "kvq_set_split_rows": (I, [P, I]),
             "kvq_set_decode_path": (I, [P, I, I]),
+            "kvq_set_softcap": (I, [P, ctypes.c_float]),
             "kvq_block_bytes": (I, [I]),
             "kvq_bytes_per_token": (S, [ctypes.POINTER(kvq_config)]),
             "kvq_last_error": (ctypes.c_char_p, []),
@@ -178,6 +180,10 @@ def kvq_set_split_rows(handle, rows):
 
 def kvq_set_decode_path(handle, path, query_bits=0):
     _check(lib().kvq_set_decode_path(handle, path, query_bits))
+
+
+def kvq_set_softcap(handle, softcap):
+    _check(lib().kvq_set_softcap(handle, float(softcap)))
 
 
 def kvq_block_bytes(fmt):

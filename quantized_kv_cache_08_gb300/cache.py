@@ -122,6 +122,10 @@ class KVCache:
     def set_split_rows(self, rows):
         B.kvq_set_split_rows(self.handle, rows)
 
+    def set_softcap(self, softcap):
+        """softcap > 0 caps scaled scores to softcap * tanh(s / softcap); 0 is off."""
+        B.kvq_set_softcap(self.handle, softcap)
+
     def set_decode_path(self, path, query_bits=0):
         """path: 0 auto, 1 generic split kernel, 2 warp-specialised kernel."""
         B.kvq_set_decode_path(self.handle, path, query_bits)

@@ -34,6 +34,7 @@ struct kvq_cache {
     int split_rows;                      // 0 = automatic
     int path;                            // 0 auto, 1 generic split kernel, 2 warp-specialised
     int nlimb;                           // query limbs of the warp-specialised kernel (2 or 3)
+    float softcap;                       // score cap (0: off)
     std::vector<int> len, base;
 };
 
@@ -192,6 +193,7 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* 
                  make_row_tensor_map(&c->vmap, v_plane, g.v_tok, (long long)cfg->n_seq * g.rows);
     c->path = 0;
     c->nlimb = 2;                          // 16-bit queries unless 24 is asked for
+    c->softcap = 0.f;
     c->len.assign(cfg->n_seq, 0);
     c->base.assign(cfg->n_seq, 0);
     e = cudaMemsetAsync(counters, 0, counters_bytes(cfg->n_seq), static_cast<cudaStream_t>(stream));
@@ -320,8 +322,10 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     // the warp-specialised kernel needs 16-byte token rows
     // (value tasks per row: a power of two from 8 to 256, so each V warp holds
     // a power-of-two number of tasks and its row groups reduce by butterfly)
+    // (no score cap: soft-capping runs on the generic kernel, so the
+    // warp-specialised kernel's hot loop carries no trace of it)
     bool fast = c->path != 1 && c->kmap_ok && 2 * nK >= 8 && 2 * nK <= 256 && ((2 * nK) & (2 * nK - 1)) == 0 &&
-                Hkv <= 8;
+                Hkv <= 8 && c->softcap == 0.f;
     if (!fast && !generic_ok)
         return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
     long long total_vis = 0;
@@ -352,6 +356,8 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     p.q = q;
     p.q_bf16 = dtype == KVQ_BF16;
     p.qscale = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
+    p.softcap_a = c->softcap > 0.f ? 1.0f / (c->softcap * 1.4426950408889634f) : 0.f;
+    p.softcap_b = c->softcap > 0.f ? c->softcap * 1.4426950408889634f : 0.f;
     p.B = B;
     p.T = T;
     p.Hq = n_q_heads;
@@ -413,7 +419,9 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         if (!fits) fast = false;
     }
     if (c->path == 2 && !fast)
-        return fail(KVQ_EUNSUPPORTED, "the warp-specialised decode does not support this geometry");
+        return fail(KVQ_EUNSUPPORTED, c->softcap > 0.f
+                                          ? "the warp-specialised decode has no score cap (use path 0 or 1)"
+                                          : "the warp-specialised decode does not support this geometry");
     if (!fast && !generic_ok)
         return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
     if (!fast && split_smem_bytes(p) > (size_t)smem_max)
@@ -551,6 +559,13 @@ kvq_status kvq_read_device_error(kvq_cache* c, int* err, void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "read error word");
     e = cudaMemset(c->err_d, 0, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+    return KVQ_OK;
+}
+
+kvq_status kvq_set_softcap(kvq_cache* c, float softcap) {
+    if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+    if (!(softcap >= 0.f) || softcap > 3.0e38f) return fail(KVQ_EINVAL, "softcap must be finite and >= 0");
+    c->softcap = softcap;
     return KVQ_OK;
 }
 

@@ -42,6 +42,14 @@ namespace {
 
 using namespace dev;
 
+// Soft-capped score in log2 units: with s = scale * <q, k> * log2(e) and
+// cap c, c * tanh(s' / c) on the natural-log score s' is b * tanh(a * s)
+// with a = 1 / (c log2 e), b = c log2 e (b == 0: no cap).
+__device__ __forceinline__ float softcap_score(const SplitParams& p, float s) {
+    if (p.softcap_b > 0.f) s = p.softcap_b * tanhf(p.softcap_a * s);
+    return s;
+}
+
 // ------------------------------------------------------------ the kernel
 
 template <int NBH, int NQG>
@@ -290,7 +298,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitPara
                                         up_n = kq_upto[m2];
                                     }
                                 const bool vis = row >= lo_n && row < up_n;
-                                Sb[r * NQ + k_g * QC + 4 * k_qg + n] = vis ? res[j] : kNegInf;
+                                Sb[r * NQ + k_g * QC + 4 * k_qg + n] = vis ? softcap_score(p, res[j]) : kNegInf;
                             }
                         }
                     }

@@ -57,6 +57,7 @@ struct SplitParams {
     const void* q;                 // [B][T][Hq][D]
     int q_bf16;
     float qscale;                  // score scale * log2(e)
+    float softcap_a, softcap_b;    // score cap in log2 units: s -> b * tanh(a * s); b == 0: off
     int B, T, Hq, Hkv, hpk, D, kb, k_tok, v_tok, max_rows, window;
     int C;                         // rows per split (multiple of kTileRows)
     int nqs;                       // query slices per (sequence, split)

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from oracle import kvq_oracle as O
-from tests.kvq_testutil import ATOL, Pair, assert_close, assert_rows_equal, need_gpu, to_dev
+from tests.kvq_testutil import ATOL, Pair, assert_close, assert_rows_equal, need_gpu, oracle_input, to_dev
 from quantized_kv_cache_08_gb300 import _binding as B
 from quantized_kv_cache_08_gb300.cache import KVCache
 
@@ -324,6 +324,50 @@ def test_ring_multi_row_chunks_match_windowed_oracle(path):
             assert_rows_equal(p.dev, p.ora, 0, lstart, L)
         step += 1
     assert step > 100 and p.dev.bases()[0] > 0
+    assert p.dev.device_error() == 0
+
+
+@pytest.mark.parametrize("path", [(0, 0), (1, 0)])
+@pytest.mark.parametrize("shape", [
+    # B, Hq, Hkv, D, lens, T, window, sinks
+    (2, 32, 8, 128, [700, 1500], 1, 0, True),
+    (1, 16, 4, 256, [600], 8, 200, False),
+])
+def test_decode_softcap_matches_oracle(shape, path):
+    """Score soft-capping (softcap 3, queries scaled up so most scores are
+    capped hard) against the oracle (it runs on the generic kernel, also
+    under automatic choice); a huge cap equals no cap, and 0 turns it off
+    again.  Forcing the warp-specialised kernel with a cap is refused."""
+    Bn, Hq, Hkv, D, lens, T, window, sinks = shape
+    p = Pair(Bn, Hkv, D, Hq, max_t=max(T, 64), max_rows=max(lens) + T, window=window)
+    p.dev.set_decode_path(*path)
+    for b, L in enumerate(lens):
+        k = _randn(1, L, Hkv, D, seed=300 + b)
+        v = _randn(1, L, Hkv, D, seed=400 + b)
+        for t0 in range(0, L, 64):
+            p.append(k[:, t0:t0 + 64], v[:, t0:t0 + 64], seq_ids=[b])
+    q = _randn(Bn, T, Hq, D, seed=17, scale=4.0)
+    s = _randn(Hq, seed=18) if sinks else None
+    plain, ref_plain = p.decode(q, sinks=s)
+    p.dev.set_softcap(3.0)
+    got = p.dev.decode(to_dev(q), sinks=None if s is None else to_dev(s)).cpu().numpy()
+    ref = p.ora.decode(oracle_input(q), sinks=None if s is None else s.double().numpy(), softcap=3.0)
+    assert_close(got, ref, what="softcap 3")
+    assert np.max(np.abs(ref - ref_plain)) > 0.05          # the cap matters here
+    p.dev.set_softcap(1e30)
+    huge = p.dev.decode(to_dev(q), sinks=None if s is None else to_dev(s)).cpu().numpy()
+    assert_close(huge, ref_plain, what="softcap 1e30")
+    p.dev.set_decode_path(2)
+    with pytest.raises(B.KvqError) as e:
+        p.dev.decode(to_dev(q))
+    assert e.value.status == B.KVQ_EUNSUPPORTED
+    p.dev.set_decode_path(*path)
+    p.dev.set_softcap(0.0)
+    again = p.dev.decode(to_dev(q), sinks=None if s is None else to_dev(s)).cpu().numpy()
+    np.testing.assert_array_equal(again, plain)
+    with pytest.raises(B.KvqError) as e:
+        p.dev.set_softcap(-1.0)
+    assert e.value.status == B.KVQ_EINVAL
     assert p.dev.device_error() == 0
 
 
