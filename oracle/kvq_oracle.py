@@ -225,6 +225,58 @@ def q5_1_dequantize(blk) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# FP8 E4M3 (the alternative K/V format: one byte per element, no block scale)
+#
+# memra-engine "Module config", entries KV_FP8_FORCE, FP8-GLOBALS switch and
+# kv_fp8_on: K and V are held as e4m3 ("kf8vf8").  The pages name the format
+# only; it is read as OCP FP8 E4M3: 1 sign bit, 4 exponent bits with bias 7,
+# 3 fraction bits, no infinities.  Normals are (1 + f/8) * 2**(E-7) for
+# E in 1..15 except E = 15, f = 7 (NaN); subnormals are f/8 * 2**-6; the
+# largest finite magnitude is 1.75 * 2**8 = 448.  Each element is encoded on
+# its own, with no scale: round to nearest, ties to even, and magnitudes
+# above 448 saturate to 448 (there is no infinity to overflow to).
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_bits(y) -> np.ndarray:
+    """Encode finite float64 values as E4M3 bytes (nearest, ties to even,
+    saturating at +-448).  Raises on non-finite input."""
+    y = np.asarray(y, dtype=np.float64)
+    if not np.all(np.isfinite(y)):
+        raise ValueError("e4m3_bits: non-finite input")
+    sign = np.signbit(y).astype(np.int64)
+    a = np.abs(y)
+    _, ex = np.frexp(a)                   # a = m * 2**ex, m in [0.5, 1); exact
+    e = np.maximum(ex.astype(np.int64) - 1, -6)    # binade; below 2**-6 the
+    quantum = np.ldexp(1.0, e - 3)                 # subnormal step 2**-9 holds
+    r = np.rint(a / quantum).astype(np.int64)      # ties to even; exact divisor
+    carry = r == 16                       # rounded up into the next binade
+    e = np.where(carry, e + 1, e)
+    r = np.where(carry, 8, r)
+    sub = r < 8                           # only possible when e == -6
+    biased = np.where(sub, 0, e + 7)
+    frac = np.where(sub, r, r - 8)
+    over = (biased > 15) | ((biased == 15) & (frac == 7))
+    biased = np.where(over, 15, biased)   # saturate to 448 = (1 + 6/8) * 2**8
+    frac = np.where(over, 6, frac)
+    return ((sign << 7) | (biased << 3) | frac).astype(np.uint8)
+
+
+def e4m3_value(bits) -> np.ndarray:
+    """Decode E4M3 bytes to float64 (exact).  0x7F and 0xFF are NaN."""
+    b = np.asarray(bits).astype(np.int64)
+    s = np.where((b >> 7) & 1, -1.0, 1.0)
+    E = (b >> 3) & 15
+    f = b & 7
+    mag = np.where(E == 0, np.ldexp(f.astype(np.float64), -9),
+                   np.ldexp((8 + f).astype(np.float64), (E - 10).astype(np.int64)))
+    mag = np.where((E == 15) & (f == 7), np.nan, mag)
+    return s * mag
+
+
+# ---------------------------------------------------------------------------
 # Token rows: [token, kv_head, dim] element order, 32-element blocks
 # ---------------------------------------------------------------------------
 
@@ -247,6 +299,20 @@ def quantize_v_rows(v, n_kv, head_dim) -> np.ndarray:
     """V rows [..., n_kv, head_dim] float32 -> [n_rows, kb*24] uint8."""
     blocks = _blocks_of_rows(v, n_kv, head_dim)
     return q5_1_quantize(blocks).reshape(blocks.shape[0], -1)
+
+
+def e4m3_rows(x, n_kv, head_dim) -> np.ndarray:
+    """K or V rows [..., n_kv, head_dim] float32 -> [n_rows, n_kv*head_dim]
+    E4M3 bytes, element e = kv_head*head_dim + d at byte e of its row."""
+    x = np.asarray(x, dtype=np.float32)
+    flat = x.reshape(-1, n_kv * head_dim).astype(np.float64)
+    return e4m3_bits(flat)
+
+
+def dequantize_e4m3_rows(rows, n_kv, head_dim) -> np.ndarray:
+    """[n_rows, n_kv*head_dim] E4M3 bytes -> float64 [n_rows, n_kv, head_dim]."""
+    rows = np.asarray(rows, dtype=np.uint8)
+    return e4m3_value(rows).reshape(rows.shape[0], n_kv, head_dim)
 
 
 def dequantize_k_rows(rows, n_kv, head_dim) -> np.ndarray:
@@ -326,15 +392,23 @@ class OracleKvCache:
     append() quantises rows exactly as the formats above state and places them
     at row `len` of each target sequence; truncate() drops rows past the new
     length (rollback: len = snapshot_len + accept_len, no copy); decode()
-    attends the last T rows of every sequence over its dequantised rows."""
+    attends the last T rows of every sequence over its dequantised rows.
+    fmt "q8_0/q5_1" stores K as q8_0 and V as q5_1 blocks; fmt "e4m3" stores
+    both as one E4M3 byte per element."""
 
-    def __init__(self, n_seq, n_kv, head_dim, window=0):
+    def __init__(self, n_seq, n_kv, head_dim, window=0, fmt="q8_0/q5_1"):
         if head_dim % QK:
             raise ValueError("head_dim must be a multiple of 32")
+        if fmt not in ("q8_0/q5_1", "e4m3"):
+            raise ValueError("fmt must be 'q8_0/q5_1' or 'e4m3'")
         self.n_seq, self.n_kv, self.head_dim, self.window = n_seq, n_kv, head_dim, window
+        self.fmt = fmt
         self.kb = n_kv * head_dim // QK
-        self.k_tok = self.kb * Q8_0_BYTES
-        self.v_tok = self.kb * Q5_1_BYTES
+        if fmt == "e4m3":
+            self.k_tok = self.v_tok = n_kv * head_dim
+        else:
+            self.k_tok = self.kb * Q8_0_BYTES
+            self.v_tok = self.kb * Q5_1_BYTES
         self._k = [np.zeros((0, self.k_tok), np.uint8) for _ in range(n_seq)]
         self._v = [np.zeros((0, self.v_tok), np.uint8) for _ in range(n_seq)]
 
@@ -350,8 +424,12 @@ class OracleKvCache:
         if k.shape[0] != len(ids) or v.shape != k.shape:
             raise ValueError("append: shape mismatch")
         for i, b in enumerate(ids):
-            kr = quantize_k_rows(k[i], self.n_kv, self.head_dim)
-            vr = quantize_v_rows(v[i], self.n_kv, self.head_dim)
+            if self.fmt == "e4m3":
+                kr = e4m3_rows(k[i], self.n_kv, self.head_dim)
+                vr = e4m3_rows(v[i], self.n_kv, self.head_dim)
+            else:
+                kr = quantize_k_rows(k[i], self.n_kv, self.head_dim)
+                vr = quantize_v_rows(v[i], self.n_kv, self.head_dim)
             self._k[b] = np.concatenate([self._k[b], kr])
             self._v[b] = np.concatenate([self._v[b], vr])
 
@@ -382,8 +460,12 @@ class OracleKvCache:
             lo = 0
             if self.window > 0:
                 lo = max(0, L - T + 1 - self.window)   # rows no query row sees
-            kh = dequantize_k_rows(self._k[b][lo:], self.n_kv, self.head_dim)
-            vh = dequantize_v_rows(self._v[b][lo:], self.n_kv, self.head_dim)
+            if self.fmt == "e4m3":
+                kh = dequantize_e4m3_rows(self._k[b][lo:], self.n_kv, self.head_dim)
+                vh = dequantize_e4m3_rows(self._v[b][lo:], self.n_kv, self.head_dim)
+            else:
+                kh = dequantize_k_rows(self._k[b][lo:], self.n_kv, self.head_dim)
+                vh = dequantize_v_rows(self._v[b][lo:], self.n_kv, self.head_dim)
             # rows before `lo` have probability exactly 0 for every query row,
             # so attending the suffix with the same window is the same result
             out[b] = attend(q[b], kh, vh, scale=scale, sinks=sinks,

@@ -5,6 +5,9 @@
 * q8_0 / q5_1 bytes: hand-derived blocks (tests/golden), an independent exact
   rational-arithmetic quantiser (fractions.Fraction), and the round-trip
   bounds |x - x_hat| <= d/2;
+* FP8 E4M3 bytes: hand-derived encodings (tests/golden), torch's
+  float8_e4m3fn decoding of every byte and encoding of in-range values (library
+  routines), and a brute-force nearest-value search over the finite codes;
 * attention: torch's scaled_dot_product_attention in float64 (an independent
   library routine) with the sink written as an extra value-less column and the
   window / causal rules written as an additive -inf mask, plus closed forms
@@ -432,3 +435,109 @@ def test_decode_window_suffix_shortcut():
     kr, vr = c.rows(0)
     full = O.attend(q[0], O.dequantize_k_rows(kr, Hkv, D), O.dequantize_v_rows(vr, Hkv, D), window=W)
     np.testing.assert_array_equal(c.decode(q)[0], full)
+
+
+# ---------------------------------------------------------------- FP8 E4M3
+
+def _torch_e4m3_table():
+    """float64 value of every E4M3 byte by torch's float8_e4m3fn decoding."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_known_encodings():
+    with open(os.path.join(GOLD, "e4m3_known.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    vals = np.array([_parse_float(r[0]) for r in rows])
+    want = np.array([int(r[1], 16) for r in rows], dtype=np.uint8)
+    np.testing.assert_array_equal(O.e4m3_bits(vals), want)
+
+
+def test_e4m3_decode_every_byte_matches_torch():
+    want = _torch_e4m3_table()
+    got = O.e4m3_value(np.arange(256))
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(want))
+    fin = ~np.isnan(want)
+    np.testing.assert_array_equal(got[fin], want[fin])
+    np.testing.assert_array_equal(np.signbit(got[fin]), np.signbit(want[fin]))
+    assert np.nanmax(got) == O.E4M3_MAX and np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+
+
+def test_e4m3_encode_is_nearest_finite_code_ties_even():
+    """Brute force: the byte of |y| is the finite non-negative code whose
+    torch-decoded value is nearest (ties to the even code), the sign bit that
+    of y; this also covers saturation beyond 448."""
+    table = _torch_e4m3_table()
+    grid = table[:0x7F]                                  # bytes 0x00..0x7E, increasing
+    rng = np.random.default_rng(21)
+    y = [np.ldexp(rng.uniform(1.0, 2.0, 40000), rng.integers(-13, 11, 40000))
+         * rng.choice([-1.0, 1.0], 40000)]
+    mids = (grid[1:] + grid[:-1]) / 2                    # every tie
+    y += [mids, -mids, np.nextafter(mids, 0), np.nextafter(mids, np.inf)]
+    y += [np.array([0.0, -0.0, 447.9, 448.0, 463.9, 464.0, 464.1, 500.0, 1e30, -1e30])]
+    y = np.concatenate(y)
+    # beyond 1000 every finite code is farther than 448; clipping there keeps
+    # the distances exact in float64
+    a = np.minimum(np.abs(y), 1000.0)
+    dist = np.abs(a[:, None] - grid[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    cand = dist == best
+    n_cand = cand.sum(axis=1)
+    assert n_cand.max() <= 2
+    first = np.argmax(cand, axis=1)
+    pick = np.where((n_cand == 2) & (first % 2 == 1), first + 1, first)
+    want = (pick | (np.signbit(y).astype(np.int64) << 7)).astype(np.uint8)
+    np.testing.assert_array_equal(O.e4m3_bits(y), want)
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    """torch's float -> float8_e4m3fn cast (round to nearest even) on float32
+    values below the 464 tie, above which torch gives NaN and the format here
+    saturates."""
+    rng = np.random.default_rng(22)
+    x = np.concatenate([rng.standard_normal(200000), 30 * rng.standard_normal(200000),
+                        np.ldexp(rng.uniform(-2, 2, 200000), rng.integers(-12, 0, 200000))])
+    x = x[np.abs(x) < 464].astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(O.e4m3_bits(x.astype(np.float64)), want)
+
+
+def test_e4m3_round_trip_and_error_bound():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    np.testing.assert_array_equal(O.e4m3_bits(O.e4m3_value(codes)), codes.astype(np.uint8))
+    rng = np.random.default_rng(23)
+    x = rng.uniform(-448, 448, 100000) * np.ldexp(1.0, rng.integers(-14, 1, 100000))
+    err = np.abs(x - O.e4m3_value(O.e4m3_bits(x)))
+    # half the spacing of the binade: 2^(max(floor(log2|x|), -6) - 4)
+    e = np.maximum(np.floor(np.log2(np.abs(x))), -6)
+    assert np.all(err <= np.ldexp(1.0, (e - 4).astype(int)))
+    with pytest.raises(ValueError):
+        O.e4m3_bits(np.array([np.inf]))
+
+
+def test_e4m3_cache_rows_and_attention_on_representable_values():
+    """With inputs that E4M3 holds exactly, the e4m3 cache stores each row as
+    its elements' bytes in [token, kv_head, dim] order and its decode equals
+    torch SDPA on the raw inputs."""
+    rng = np.random.default_rng(24)
+    table = _torch_e4m3_table()
+    fin = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    n_seq, L, Hkv, D, Hq, T = 2, 40, 2, 64, 8, 3
+    kc = rng.choice(fin[np.abs(table[fin]) <= 4], (n_seq, L, Hkv, D))
+    vc = rng.choice(fin, (n_seq, L, Hkv, D))
+    k, v = table[kc].astype(np.float32), table[vc].astype(np.float32)
+    c = O.OracleKvCache(n_seq, Hkv, D, fmt="e4m3")
+    assert c.k_tok == c.v_tok == Hkv * D
+    c.append(k[:, :25], v[:, :25])
+    c.append(k[:, 25:], v[:, 25:])
+    for b in range(n_seq):
+        kr, vr = c.rows(b)
+        np.testing.assert_array_equal(kr, kc[b].reshape(L, -1).astype(np.uint8))
+        np.testing.assert_array_equal(vr, vc[b].reshape(L, -1).astype(np.uint8))
+    q = rng.standard_normal((n_seq, T, Hq, D)) * 0.1
+    sinks = rng.standard_normal(Hq)
+    got = c.decode(q, sinks=sinks)
+    for b in range(n_seq):
+        ref = _sdpa_reference(q[b], k[b].astype(np.float64), v[b].astype(np.float64),
+                              scale=1 / math.sqrt(D), sinks=sinks, window=0)
+        np.testing.assert_allclose(got[b], ref, rtol=1e-11, atol=1e-11)
