@@ -10,14 +10,15 @@ step: the captured K-step graph minus the same graph without the decodes, both
 timed by CUDA events around the replay on the launching stream.
 
 `value` is GB/s of quantised KV read by the decode (algorithmic bytes: every
-visible row x (K 34 + V 24 bytes per 32 elements)), summed over all ranks.
+visible row x (K 34 + V 24 bytes per 32 elements, or 32 + 32 with
+--kv-format e4m3)), summed over all ranks.
 `e2e` repeats the step through the same public API with the step's inputs
 copied from pinned host memory and the attention output copied back inside
 the timed region.  `--impl reference` times the fp64 CPU oracle on a bounded
 sample of the same workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-       [--layers R] [--impl kvq|reference]
+       [--layers R] [--kv-format q8_0/q5_1|e4m3] [--impl kvq|reference]
 """
 
 from __future__ import annotations
@@ -44,9 +45,12 @@ METRIC = "decode-attn GB/s of quantized KV read (fraction of HBM peak); tokens/s
 L2_BYTES = 129 * 1024 * 1024
 
 
-def kv_bytes_per_row(wl):
+FORMATS = {"q8_0/q5_1": ("K q8_0 / V q5_1", 34 + 24), "e4m3": ("K, V fp8 e4m3", 32 + 32)}
+
+
+def kv_bytes_per_row(wl, fmt="q8_0/q5_1"):
     kb = wl.n_kv * wl.head_dim // 32
-    return kb * (34 + 24)
+    return kb * FORMATS[fmt][1]
 
 
 def decode_lengths(wl):
@@ -186,7 +190,8 @@ def run_kvq(args, world, rank, local):
     wl = workload(args.workload)
     T = wl.T
     lens = decode_lengths(wl)
-    row_bytes = kv_bytes_per_row(wl)
+    fmt = args.kv_format
+    row_bytes = kv_bytes_per_row(wl, fmt)
     vis = [visible_rows(wl, L) for L in lens]
     footprint = sum(vis) * row_bytes
     R = args.layers or min(8, max(1, math.ceil(3 * L2_BYTES / footprint)))
@@ -202,10 +207,11 @@ def run_kvq(args, world, rank, local):
     caches = []
     for r in range(R):
         if wl.ring:
-            c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=T, window=wl.window, ring=True)
+            c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=T, window=wl.window, ring=True,
+                        fmt=fmt)
         else:
             c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=64, max_rows=max(lens),
-                        window=wl.window)
+                        window=wl.window, fmt=fmt)
         chunk = T if wl.ring else 64
         for b, L in enumerate(lens):
             k, v = wl.kv(b + 1000 * r + 100000 * rank, 0, L - T + 64 * T)
@@ -376,7 +382,7 @@ def run_kvq(args, world, rank, local):
         extra += ", a sink logit per Q head"
     cfg = {"workload": f"{wl.name}: {wl.n_seq} seq, {wl.n_q} Q / {wl.n_kv} KV heads, head_dim "
                        f"{wl.head_dim}, {sum(lens)} rows at decode, T={T}{extra}, q {wl.q_dtype}, "
-                       f"K q8_0 / V q5_1",
+                       f"{FORMATS[fmt][0]}",
            "layers": R, "rows_total": sum(lens), "rows_visible": sum(vis),
            "kv_bytes_per_decode": footprint,
            "step": f"per layer: append {T} row(s) + decode + truncate back",
@@ -393,7 +399,8 @@ def run_kvq(args, world, rank, local):
         "decode_ms_per_layer": round(dec_ms / decodes, 5),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
+                     "traffic": recorded_traffic(wl.name if fmt == "q8_0/q5_1" else f"{wl.name}:{fmt}"),
+                     "peak_source": peak_src,
                      "kernel": "kvq decode (split + merge)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4),
@@ -409,11 +416,11 @@ def run_kvq(args, world, rank, local):
         "clocks": clk,
     }
     if rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(wl, lens, sinks=sinks)
+        line["cpu_baseline"] = cpu_baseline(wl, lens, sinks=sinks, fmt=fmt)
     return line
 
 
-def cpu_baseline(wl, lens, budget_s=12.0, sinks=None):
+def cpu_baseline(wl, lens, budget_s=12.0, sinks=None, fmt="q8_0/q5_1"):
     """The fp64 oracle, as it stands, on a bounded sample of the workload: the
     decode of one layer for the first sequence (quantise its rows once, then
     dequantise + attend per repetition)."""
@@ -421,7 +428,7 @@ def cpu_baseline(wl, lens, budget_s=12.0, sinks=None):
 
     L = lens[0]
     k, v = wl.kv(0, 0, L)
-    ora = O.OracleKvCache(1, wl.n_kv, wl.head_dim, window=wl.window)
+    ora = O.OracleKvCache(1, wl.n_kv, wl.head_dim, window=wl.window, fmt=fmt)
     ora.append(k.unsqueeze(0).numpy(), v.unsqueeze(0).numpy())
     q = wl.q(0)[:1].float().numpy().astype("float64")
     sk = None if sinks is None else sinks.double().numpy()
@@ -431,7 +438,7 @@ def cpu_baseline(wl, lens, budget_s=12.0, sinks=None):
         ora.decode(q, sinks=sk)
         t_total += time.perf_counter() - t
         reps += 1
-    gbs = reps * visible_rows(wl, L) * kv_bytes_per_row(wl) / t_total / 1e9
+    gbs = reps * visible_rows(wl, L) * kv_bytes_per_row(wl, fmt) / t_total / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{reps} fp64 decodes of 1 sequence x {visible_rows(wl, L)} visible rows ({wl.name}), "
                       f"numpy with its default BLAS threading, {t_total:.1f} s"}
@@ -444,11 +451,12 @@ def run_reference(args, world, rank):
     wl = workload(args.workload)
     lens = decode_lengths(wl)
     base = cpu_baseline(wl, lens, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)),
-                        sinks=wl.sink_logits())
+                        sinks=wl.sink_logits(), fmt=args.kv_format)
     return {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "sample": base["sample"]},
+            "data": "synthetic", "config": {"workload": wl.name, "kv_format": args.kv_format,
+                                            "sample": base["sample"]},
             "cpu_baseline": base,
             "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -461,6 +469,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="ctx32k")
     ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--kv-format", default="q8_0/q5_1", choices=sorted(FORMATS),
+                    help="K/V storage: q8_0 K with q5_1 V (default), or FP8 E4M3 K and V")
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     args = ap.parse_args()
     if args.warmup < 3:

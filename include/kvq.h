@@ -1,6 +1,7 @@
 /*
  * kvq.h - C ABI of a GPU-resident quantised KV cache for one attention layer
- * holding B sequences: K stored q8_0, V stored q5_1, with quantised append,
+ * holding B sequences: K stored q8_0 and V stored q5_1 (or both stored FP8
+ * E4M3, one byte per element), with quantised append,
  * truncate-based rollback and split-K flash-decode attention (GQA fan-out,
  * learned sinks, sliding window over a rebased ring, T >= 1 causal rows).
  *
@@ -71,8 +72,14 @@ typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype;
  *             code i), 16 bytes qs (byte j = code j low nibble | code j+16
  *             low nibble << 4); codes round-half-away((x-m)/d) in [0,31]
  *             against the stored m and d                                24 B
- * All multi-byte fields are little-endian. */
-typedef enum kvq_fmt { KVQ_Q8_0 = 0, KVQ_Q5_1 = 1 } kvq_fmt;
+ *   KVQ_FP8_E4M3: one byte per element, no scale (memra-engine "Module
+ *             config", FP8-GLOBALS switch and kv_fp8_on: K/V held in e4m3).
+ *             Read as OCP FP8 E4M3: sign, 4 exponent bits with bias 7, 3
+ *             fraction bits, no infinities, largest finite 448; round to
+ *             nearest, ties to even, magnitudes above 448 saturate to 448.
+ *             A 32-element block is 32 bytes.
+ * All multi-byte fields are little-endian.  Inputs must be finite. */
+typedef enum kvq_fmt { KVQ_Q8_0 = 0, KVQ_Q5_1 = 1, KVQ_FP8_E4M3 = 2 } kvq_fmt;
 
 typedef struct kvq_config {
     int n_seq;        /* B: sequences held by this layer cache (1..4096)           */
@@ -86,8 +93,8 @@ typedef struct kvq_config {
                       /* last `window` rows up to and including its own row        */
     int ring;         /* 1: SWA ring addressing, physical = row - base (needs      */
                       /* window > 0); 0: flat rows [0, max_rows)                   */
-    kvq_fmt k_fmt;    /* must be KVQ_Q8_0                                          */
-    kvq_fmt v_fmt;    /* must be KVQ_Q5_1                                          */
+    kvq_fmt k_fmt;    /* KVQ_Q8_0 with v_fmt KVQ_Q5_1, or KVQ_FP8_E4M3 with        */
+    kvq_fmt v_fmt;    /* v_fmt KVQ_FP8_E4M3; no other pairs                        */
 } kvq_config;
 
 /* Device bytes the caller provides (each buffer 16-byte aligned):
@@ -95,6 +102,7 @@ typedef struct kvq_config {
  *             128 bytes of padding (tile copies move whole 128-byte column
  *             blocks), rounded up to a multiple of 256 bytes
  *   v_plane   [n_seq][max_rows][kb*24]  (padded and rounded likewise)
+ *             With FP8 E4M3 both planes are [n_seq][max_rows][kb*32].
  *   counters  len_d[n_seq], base_d[n_seq], error word, work-item counter (int32)
  *   workspace decode partials, the split plan and the ring-rebase scratch   */
 typedef struct kvq_sizes {
@@ -107,7 +115,8 @@ typedef struct kvq_cache kvq_cache;
 kvq_status kvq_required_bytes(const kvq_config* cfg, kvq_sizes* out);
 
 /* Build a cache over caller buffers (fn new of "Struct Cache").  Validates the
- * geometry (head_dim % 32 == 0, formats q8_0/q5_1, ring needs window > 0),
+ * geometry (head_dim % 32 == 0, formats q8_0/q5_1 or e4m3/e4m3, ring needs
+ * window > 0),
  * checks 16-byte alignment, and enqueues on `stream` the zeroing of the
  * counters (len = 0, base = 0, error = 0).  Byte planes are not cleared:
  * rows at or beyond a sequence's length are never read.  `*out` receives a
@@ -200,11 +209,13 @@ kvq_status kvq_physical_rows(const kvq_cache* cache, int seq, int start,
 kvq_status kvq_read_device_error(kvq_cache* cache, int* err, void* stream);
 
 /* Choose the decode kernel: path 0 = automatic (the warp-specialised kernel
- * whenever token rows are 16-byte multiples, n_kv_heads <= 8,
+ * whenever the formats are q8_0/q5_1, token rows are 16-byte multiples,
+ * n_kv_heads <= 8,
  * (queries per KV head rounded up to 4 or 8) / 4 * n_kv_heads * head_dim / 32
  * is a power of two <= 128, and its tiles fit shared memory, else the generic
  * split kernel), 1 = generic, 2 = warp-specialised
- * (KVQ_EUNSUPPORTED at decode time if the geometry does not allow it).
+ * (KVQ_EUNSUPPORTED at decode time if the geometry or format does not allow
+ * it; FP8 E4M3 caches always decode on the generic kernel).
  * query_bits (0 = 16, or 16, or 24): the warp-specialised kernel quantises
  * each pre-scaled query element per 32-element block to this many bits
  * against the block's largest magnitude and multiplies with int8 dot
@@ -226,8 +237,8 @@ kvq_status kvq_set_softcap(kvq_cache* cache, float softcap);
 /* Override the decode split size in rows (a multiple of 8, >= 64; 0 = auto). */
 kvq_status kvq_set_split_rows(kvq_cache* cache, int rows);
 
-/* Bytes per 32-element block of a format: 34 (q8_0) or 24 (q5_1); -1 if
- * unknown ("Module cache", fn kv_blk_bytes). */
+/* Bytes per 32-element block of a format: 34 (q8_0), 24 (q5_1) or 32
+ * (FP8 E4M3); -1 if unknown ("Module cache", fn kv_blk_bytes). */
 int kvq_block_bytes(kvq_fmt fmt);
 
 /* Context-linear bytes one token occupies in this layer cache, K plus V

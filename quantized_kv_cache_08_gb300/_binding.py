@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(HERE, "libkvq.so")
 KVQ_OK, KVQ_EINVAL, KVQ_ERANGE, KVQ_ECUDA, KVQ_EUNSUPPORTED = 0, 1, 2, 3, 4
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 KVQ_F32, KVQ_BF16 = 0, 1
-KVQ_Q8_0, KVQ_Q5_1 = 0, 1
+KVQ_Q8_0, KVQ_Q5_1, KVQ_FP8_E4M3 = 0, 1, 2
 
 STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ERANGE", 3: "KVQ_ECUDA", 4: "KVQ_EUNSUPPORTED"}
 
@@ -103,9 +103,10 @@ def _ints(xs):
     return arr
 
 
-def make_config(n_seq, n_kv_heads, head_dim, max_q_heads, max_t=1, max_rows=0, window=0, ring=0):
+def make_config(n_seq, n_kv_heads, head_dim, max_q_heads, max_t=1, max_rows=0, window=0, ring=0,
+                k_fmt=KVQ_Q8_0, v_fmt=KVQ_Q5_1):
     return kvq_config(n_seq, n_kv_heads, head_dim, max_q_heads, max_t, max_rows, window,
-                      int(bool(ring)), KVQ_Q8_0, KVQ_Q5_1)
+                      int(bool(ring)), k_fmt, v_fmt)
 
 
 def kvq_required_bytes(cfg):

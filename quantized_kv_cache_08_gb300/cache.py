@@ -33,13 +33,20 @@ def _check_dev(t, name):
 
 
 class KVCache:
-    """n_seq sequences of one attention layer: q8_0 K plane, q5_1 V plane,
-    device counters and the decode workspace, all caller-owned torch memory."""
+    """n_seq sequences of one attention layer: q8_0 K plane and q5_1 V plane
+    (fmt "q8_0/q5_1") or FP8 E4M3 K and V planes (fmt "e4m3"), device counters
+    and the decode workspace, all caller-owned torch memory."""
+
+    FORMATS = {"q8_0/q5_1": (B.KVQ_Q8_0, B.KVQ_Q5_1, 34, 24), "e4m3": (B.KVQ_FP8_E4M3, B.KVQ_FP8_E4M3, 32, 32)}
 
     def __init__(self, n_seq, n_kv_heads, head_dim, max_q_heads, max_t=1, max_rows=0,
-                 window=0, ring=False, device=None, stream=None):
+                 window=0, ring=False, device=None, stream=None, fmt="q8_0/q5_1"):
+        if fmt not in self.FORMATS:
+            raise ValueError(f"fmt must be one of {sorted(self.FORMATS)}")
+        k_fmt, v_fmt, k_blk, v_blk = self.FORMATS[fmt]
+        self.fmt = fmt
         self.cfg = B.make_config(n_seq, n_kv_heads, head_dim, max_q_heads, max_t, max_rows,
-                                 window, ring)
+                                 window, ring, k_fmt, v_fmt)
         sz = B.kvq_required_bytes(self.cfg)
         dev = torch.device("cuda") if device is None else torch.device(device)
         self.k_plane = torch.empty(sz.k_plane, dtype=torch.uint8, device=dev)
@@ -48,7 +55,7 @@ class KVCache:
         self.workspace = torch.empty(max(sz.workspace, 16), dtype=torch.uint8, device=dev)
         self.n_seq, self.n_kv_heads, self.head_dim = n_seq, n_kv_heads, head_dim
         kb = n_kv_heads * head_dim // 32
-        self.k_tok, self.v_tok = kb * 34, kb * 24
+        self.k_tok, self.v_tok = kb * k_blk, kb * v_blk
         if ring:
             self.rows = max_rows if max_rows else window + 30 + max_t
         else:

@@ -34,6 +34,7 @@ struct kvq_cache {
     int split_rows;                      // 0 = automatic
     int path;                            // 0 auto, 1 generic split kernel, 2 warp-specialised
     int nlimb;                           // query limbs of the warp-specialised kernel (2 or 3)
+    int fp8;                             // 1: K and V planes hold FP8 E4M3 bytes
     float softcap;                       // score cap (0: off)
     std::vector<int> len, base;
 };
@@ -59,13 +60,14 @@ kvq_status cuda_fail(cudaError_t e, const char* what) {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Geometry {
-    int kb, k_tok, v_tok, rows, max_vis;
+    int kb, k_tok, v_tok, rows, max_vis, fp8;
 };
 
 kvq_status check_config(const kvq_config* c, Geometry* g) {
     if (!c) return fail(KVQ_EINVAL, "config is NULL");
-    if (c->k_fmt != KVQ_Q8_0 || c->v_fmt != KVQ_Q5_1)
-        return fail(KVQ_EUNSUPPORTED, "formats must be K=q8_0, V=q5_1");
+    const bool q8q5 = c->k_fmt == KVQ_Q8_0 && c->v_fmt == KVQ_Q5_1;
+    const bool f8 = c->k_fmt == KVQ_FP8_E4M3 && c->v_fmt == KVQ_FP8_E4M3;
+    if (!q8q5 && !f8) return fail(KVQ_EUNSUPPORTED, "formats must be K=q8_0, V=q5_1 or K=V=fp8_e4m3");
     if (c->n_seq < 1 || c->n_seq > 4096) return fail(KVQ_EINVAL, "n_seq must be in [1, 4096]");
     if (c->n_kv_heads < 1) return fail(KVQ_EINVAL, "n_kv_heads must be >= 1");
     if (c->head_dim < 32 || c->head_dim > 512 || c->head_dim % 32)
@@ -78,8 +80,9 @@ kvq_status check_config(const kvq_config* c, Geometry* g) {
     const long long kvd = (long long)c->n_kv_heads * c->head_dim;
     if (kvd > 65536) return fail(KVQ_EINVAL, "n_kv_heads * head_dim too large");
     g->kb = (int)(kvd / kQK);
-    g->k_tok = g->kb * kQ8Bytes;
-    g->v_tok = g->kb * kQ5Bytes;
+    g->fp8 = f8 ? 1 : 0;
+    g->k_tok = g->kb * (f8 ? kF8Bytes : kQ8Bytes);
+    g->v_tok = g->kb * (f8 ? kF8Bytes : kQ5Bytes);
     if (c->ring) {
         const int need = c->window + 30 + c->max_t;
         g->rows = c->max_rows == 0 ? need : c->max_rows;
@@ -128,6 +131,7 @@ const char* kvq_last_error(void) { return g_err.c_str(); }
 int kvq_block_bytes(kvq_fmt fmt) {
     if (fmt == KVQ_Q8_0) return kQ8Bytes;
     if (fmt == KVQ_Q5_1) return kQ5Bytes;
+    if (fmt == KVQ_FP8_E4M3) return kF8Bytes;
     return -1;
 }
 
@@ -193,6 +197,7 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* 
                  make_row_tensor_map(&c->vmap, v_plane, g.v_tok, (long long)cfg->n_seq * g.rows);
     c->path = 0;
     c->nlimb = 2;                          // 16-bit queries unless 24 is asked for
+    c->fp8 = g.fp8;
     c->softcap = 0.f;
     c->len.assign(cfg->n_seq, 0);
     c->base.assign(cfg->n_seq, 0);
@@ -282,6 +287,7 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, kvq_dtype dtyp
     p.k_tok = c->k_tok;
     p.v_tok = c->v_tok;
     p.max_rows = c->rows;
+    p.fp8 = c->fp8;
     SeqIds sid;
     for (size_t first = 0; first < ids.size(); first += kMaxIdsPerLaunch) {
         const int n = (int)std::min(ids.size() - first, (size_t)kMaxIdsPerLaunch);
@@ -324,7 +330,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     // a power-of-two number of tasks and its row groups reduce by butterfly)
     // (no score cap: soft-capping runs on the generic kernel, so the
     // warp-specialised kernel's hot loop carries no trace of it)
-    bool fast = c->path != 1 && c->kmap_ok && 2 * nK >= 8 && 2 * nK <= 256 && ((2 * nK) & (2 * nK - 1)) == 0 &&
+    bool fast = c->path != 1 && !c->fp8 && c->kmap_ok && 2 * nK >= 8 && 2 * nK <= 256 && ((2 * nK) & (2 * nK - 1)) == 0 &&
                 Hkv <= 8 && c->softcap == 0.f;
     if (!fast && !generic_ok)
         return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
@@ -369,6 +375,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     p.v_tok = c->v_tok;
     p.max_rows = c->rows;
     p.window = c->cfg.window;
+    p.fp8 = c->fp8;
     p.C = C;
     p.QC = QC;
     p.nqs = (Q + QC - 1) / QC;
@@ -419,7 +426,8 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         if (!fits) fast = false;
     }
     if (c->path == 2 && !fast)
-        return fail(KVQ_EUNSUPPORTED, c->softcap > 0.f
+        return fail(KVQ_EUNSUPPORTED, c->fp8 ? "the warp-specialised decode reads q8_0/q5_1 only (use path 0 or 1)"
+                                      : c->softcap > 0.f
                                           ? "the warp-specialised decode has no score cap (use path 0 or 1)"
                                           : "the warp-specialised decode does not support this geometry");
     if (!fast && !generic_ok)

@@ -1,4 +1,5 @@
-// Quantised append (q8_0 K, q5_1 V) and the small counter kernels.
+// Quantised append (q8_0 K, q5_1 V, or FP8 E4M3 K and V) and the small
+// counter kernels.
 //
 // Formats and row placement: memra-engine "Struct KvLayer" (type
 // description): a token row keeps the [token, kv_head, dim] element order, so
@@ -15,10 +16,16 @@
 // is below 2e-5 of a code step; only when the estimate lies within 1e-3 of a
 // rounding boundary does it recompute the quotient in fp64 exactly as the
 // definition reads, so every code equals the fp64 decision.
+//
+// FP8 E4M3 (memra-engine "Module config", FP8-GLOBALS switch and kv_fp8_on:
+// K/V held in e4m3): each element becomes one byte on its own, with no scale,
+// by the hardware conversion that rounds to nearest even and saturates to
+// +-448 (cvt.rn.satfinite); byte e of a token row is element e.
 #include "kvq_internal.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 namespace kvq {
 namespace {
@@ -102,6 +109,13 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p, SeqIds ids,
     const float xk = load_elem(p.k, src, p.bf16);
     const float xv = load_elem(p.v, src, p.bf16);
     const long long row = (long long)b * p.max_rows + phys;
+
+    if (p.fp8) {
+        const long long e = (long long)j * kQK + lane;
+        p.k_plane[row * p.k_tok + e] = __nv_cvt_float_to_fp8(xk, __NV_SATFINITE, __NV_E4M3);
+        p.v_plane[row * p.v_tok + e] = __nv_cvt_float_to_fp8(xv, __NV_SATFINITE, __NV_E4M3);
+        return;
+    }
 
     // ---- K: q8_0 ----
     {

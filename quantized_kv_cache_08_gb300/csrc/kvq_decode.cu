@@ -32,6 +32,12 @@
 //            arithmetic and placed into the mantissa of 0.5 (value 0.5+u/256),
 //            so v_hat = 256 d * F + (m - 128 d) and o += (p*256d) F by packed
 //            FMAs, with sum p*(m - 128 d) kept per block.
+// FP8 E4M3 planes (memra-engine "Module config", kv_fp8_on: K/V held in e4m3)
+// take the same phases with one byte per element and no block fields: a byte
+// moved into the sign, exponent and top fraction bits of a binary16 value is
+// the E4M3 value times 2^-8 (the exponent biases are 15 and 7, and subnormals
+// line up too), so both phases convert bytes in pairs through half2 and fold
+// the 2^8 into the key score and the value weight.
 // At the end of an item the V row groups are summed through shared memory and
 // the partial (max, sum, o[D]) of every query is written out; the merge
 // kernel combines the partials of a sequence with the sink by log-sum-exp.
@@ -50,9 +56,25 @@ __device__ __forceinline__ float softcap_score(const SplitParams& p, float s) {
     return s;
 }
 
+// Four E4M3 bytes of a little-endian word (elements 0..3) as floats scaled by
+// 2^-8: byte b becomes the binary16 bits (b & 0x80) << 8 | (b & 0x7f) << 7.
+__device__ __forceinline__ void e4m3x4_scaled(uint32_t w, float2& f01, float2& f23) {
+    const uint32_t lo = __byte_perm(w, 0, 0x4140);   // byte 0 | byte 1 << 16
+    const uint32_t hi = __byte_perm(w, 0, 0x4342);   // byte 2 | byte 3 << 16
+    __half2_raw a, b;
+    const uint32_t ha = ((lo << 8) & 0x80008000u) | ((lo << 7) & 0x3F803F80u);
+    const uint32_t hb = ((hi << 8) & 0x80008000u) | ((hi << 7) & 0x3F803F80u);
+    a.x = (unsigned short)(ha & 0xffffu);
+    a.y = (unsigned short)(ha >> 16);
+    b.x = (unsigned short)(hb & 0xffffu);
+    b.y = (unsigned short)(hb >> 16);
+    f01 = __half22float2(__half2(a));
+    f23 = __half22float2(__half2(b));
+}
+
 // ------------------------------------------------------------ the kernel
 
-template <int NBH, int NQG>
+template <int NBH, int NQG, bool F8>
 __global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitParams p) {
     constexpr int QC = 4 * NQG;                    // queries per KV group per slice
     extern __shared__ __align__(128) uint8_t smem[];
@@ -220,7 +242,34 @@ __global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitPara
                 for (int k = 0; k < iters; ++k) {
                     const int r = k_rg + k * rpK;
                     float sc[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (r < nr) {
+                    if constexpr (F8) {
+                        if (r < nr) {
+                            // 32 bytes of the block, 16-byte aligned (k_tok is a multiple of 32)
+                            const uint32_t a = ktile + (uint32_t)(r * p.k_tok + k_blk * kF8Bytes);
+                            uint32_t w[8];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const uint2 t = lds64(a + 8 * i);
+                                w[2 * i] = t.x;
+                                w[2 * i + 1] = t.y;
+                            }
+                            float2 acc[4];
+#pragma unroll
+                            for (int n = 0; n < 4; ++n) acc[n] = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                float2 f01, f23;
+                                e4m3x4_scaled(w[i], f01, f23);
+#pragma unroll
+                                for (int n = 0; n < 4; ++n) {
+                                    acc[n] = __ffma2_rn(qv[n][2 * i], f01, acc[n]);
+                                    acc[n] = __ffma2_rn(qv[n][2 * i + 1], f23, acc[n]);
+                                }
+                            }
+#pragma unroll
+                            for (int n = 0; n < 4; ++n) sc[n] = (acc[n].x + acc[n].y) * 256.f;
+                        }
+                    } else if (r < nr) {
                         const uint32_t a = ktile + (uint32_t)(r * p.k_tok + k_blk * kQ8Bytes);
                         const uint32_t a0 = a & ~3u;
                         const bool odd = (a & 2u) != 0;          // block starts at 2 mod 4
@@ -357,6 +406,30 @@ __global__ void __launch_bounds__(kSplitThreads, 1) split_kernel(const SplitPara
                     }
                 }
                 const uint32_t sb = smem_u32(Sb);
+                if constexpr (F8) {
+                    // dims 8hf..8hf+7 and 16+8hf..16+8hf+7 of the block, as in the q5_1 case
+                    for (int r = v_rg; r < nr; r += rpV) {
+                        const uint32_t vb = vtile + (uint32_t)(r * p.v_tok + v_blk * kF8Bytes + 8 * v_hf);
+                        const uint2 x0 = lds64(vb);
+                        const uint2 x1 = lds64(vb + 16);
+                        const float4 p4 = lds128f(sb + 4u * (uint32_t)(r * NQ + v_qq0));
+                        const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
+                        const uint32_t u[4] = {x0.x, x0.y, x1.x, x1.y};
+                        float2 pd[4];
+#pragma unroll
+                        for (int n = 0; n < 4; ++n) pd[n] = make_float2(pr[n] * 256.f, pr[n] * 256.f);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            float2 fa, fb;
+                            e4m3x4_scaled(u[c], fa, fb);
+#pragma unroll
+                            for (int n = 0; n < 4; ++n) {
+                                o2[n][2 * c] = __ffma2_rn(pd[n], fa, o2[n][2 * c]);
+                                o2[n][2 * c + 1] = __ffma2_rn(pd[n], fb, o2[n][2 * c + 1]);
+                            }
+                        }
+                    }
+                } else
                 for (int r = v_rg; r < nr; r += rpV) {
                     const uint32_t vb = vtile + (uint32_t)(r * p.v_tok + v_blk * kQ5Bytes);
                     const uint2 dmqh = lds64(vb);
@@ -585,9 +658,9 @@ __global__ void __launch_bounds__(merge_threads(VPL)) merge_kernel(const MergePa
     }
 }
 
-template <int NBH, int NQG>
+template <int NBH, int NQG, bool F8>
 cudaError_t launch_split_t(const SplitParams& p, int grid, size_t smem, cudaStream_t s) {
-    auto fn = split_kernel<NBH, NQG>;
+    auto fn = split_kernel<NBH, NQG, F8>;
     static std::atomic<unsigned long long> attrs{0};
     cudaError_t e = kernel_attrs_once(fn, attrs, false);
     if (e != cudaSuccess) return e;
@@ -622,8 +695,9 @@ int split_max_smem() {
 cudaError_t launch_split(const SplitParams& p, int grid, cudaStream_t s) {
     const size_t smem = split_smem_bytes(p);
     const int NBH = p.D / 32, NQG = p.QC / 4;
-#define KVQ_CASE(nb, nq) \
-    if (NBH == nb && NQG == nq) return launch_split_t<nb, nq>(p, grid, smem, s);
+#define KVQ_CASE(nb, nq)                                                                        \
+    if (NBH == nb && NQG == nq)                                                                 \
+        return p.fp8 ? launch_split_t<nb, nq, true>(p, grid, smem, s) : launch_split_t<nb, nq, false>(p, grid, smem, s);
     KVQ_CASE(1, 1) KVQ_CASE(2, 1) KVQ_CASE(4, 1) KVQ_CASE(8, 1) KVQ_CASE(16, 1)
     KVQ_CASE(1, 2) KVQ_CASE(2, 2) KVQ_CASE(4, 2) KVQ_CASE(8, 2) KVQ_CASE(16, 2)
 #undef KVQ_CASE

@@ -14,6 +14,7 @@ namespace kvq {
 constexpr int kQK = 32;            // elements per quantisation block
 constexpr int kQ8Bytes = 34;       // q8_0 block: fp16 d + 32 int8 codes
 constexpr int kQ5Bytes = 24;       // q5_1 block: fp16 d, fp16 m, u32 qh, 16 B qs
+constexpr int kF8Bytes = 32;       // 32 FP8 E4M3 elements, no scale
 constexpr int kMaxIdsPerLaunch = 256;
 constexpr int kSplitThreads = 256; // decode split CTA size
 constexpr int kTileRows = 16;      // KV rows staged per pipeline stage
@@ -44,6 +45,7 @@ struct AppendParams {
     const int* base_d;
     int* err_d;
     int T, kb, k_tok, v_tok, max_rows;
+    int fp8;                       // 1: both planes hold FP8 E4M3 bytes
     long long entry_offset;        // first input entry of this launch
 };
 
@@ -59,6 +61,7 @@ struct SplitParams {
     float qscale;                  // score scale * log2(e)
     float softcap_a, softcap_b;    // score cap in log2 units: s -> b * tanh(a * s); b == 0: off
     int B, T, Hq, Hkv, hpk, D, kb, k_tok, v_tok, max_rows, window;
+    int fp8;                       // 1: both planes hold FP8 E4M3 bytes (generic kernel only)
     int C;                         // rows per split (multiple of kTileRows)
     int nqs;                       // query slices per (sequence, split)
     int QC;                        // queries per KV group per slice

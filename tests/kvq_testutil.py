@@ -53,10 +53,11 @@ def assert_close(got, want, atol=ATOL, what="output"):
 class Pair:
     """A device cache and an oracle cache fed with identical inputs."""
 
-    def __init__(self, n_seq, n_kv, head_dim, n_q, max_t=1, max_rows=0, window=0, ring=False):
+    def __init__(self, n_seq, n_kv, head_dim, n_q, max_t=1, max_rows=0, window=0, ring=False,
+                 fmt="q8_0/q5_1"):
         self.dev = KVCache(n_seq, n_kv, head_dim, n_q, max_t=max_t, max_rows=max_rows,
-                           window=window, ring=ring)
-        self.ora = O.OracleKvCache(n_seq, n_kv, head_dim, window=window)
+                           window=window, ring=ring, fmt=fmt)
+        self.ora = O.OracleKvCache(n_seq, n_kv, head_dim, window=window, fmt=fmt)
         self.n_seq, self.n_kv, self.head_dim, self.n_q = n_seq, n_kv, head_dim, n_q
 
     def append(self, k, v, seq_ids=None):

@@ -41,6 +41,7 @@ def test_library_exports_every_declared_symbol(L):
 def test_block_bytes(L):
     assert B.kvq_block_bytes(B.KVQ_Q8_0) == 34
     assert B.kvq_block_bytes(B.KVQ_Q5_1) == 24
+    assert B.kvq_block_bytes(B.KVQ_FP8_E4M3) == 32
     assert B.kvq_block_bytes(7) == -1
 
 
@@ -61,6 +62,12 @@ def test_bytes_per_token_and_required_sizes(L):
     # bytes so whole-block tile copies stay inside
     assert sz.k_plane == -(-(4127 * 16 * 34 + 128) // 256) * 256
     assert sz.v_plane == -(-(4127 * 16 * 24 + 128) // 256) * 256
+    # FP8 E4M3: one byte per element in both planes
+    f8 = B.make_config(1, 8, 128, 32, max_t=1, max_rows=32768, k_fmt=B.KVQ_FP8_E4M3,
+                       v_fmt=B.KVQ_FP8_E4M3)
+    assert B.kvq_bytes_per_token(f8) == 2 * 1024
+    sz = B.kvq_required_bytes(f8)
+    assert sz.k_plane == sz.v_plane == 32768 * 1024 + 256
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -88,9 +95,12 @@ def test_invalid_configs_rejected(L, kw, status):
     assert e.value.status == status
 
 
-def test_wrong_formats_unsupported(L):
-    cfg = B.make_config(1, 2, 128, 8, max_rows=64)
-    cfg.k_fmt = B.KVQ_Q5_1
+@pytest.mark.parametrize("k_fmt,v_fmt", [
+    (B.KVQ_Q5_1, B.KVQ_Q5_1), (B.KVQ_Q5_1, B.KVQ_Q8_0), (B.KVQ_FP8_E4M3, B.KVQ_Q5_1),
+    (B.KVQ_Q8_0, B.KVQ_FP8_E4M3), (9, 9),
+])
+def test_wrong_formats_unsupported(L, k_fmt, v_fmt):
+    cfg = B.make_config(1, 2, 128, 8, max_rows=64, k_fmt=k_fmt, v_fmt=v_fmt)
     with pytest.raises(B.KvqError) as e:
         B.kvq_required_bytes(cfg)
     assert e.value.status == B.KVQ_EUNSUPPORTED
