@@ -28,6 +28,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -80,10 +81,15 @@ def measured_peak():
 
 
 def kernel_source_hash():
+    """Hash of the CUDA sources with their comments removed, so that recorded
+    counters stay valid across comment-only edits and no longer."""
     h = hashlib.sha256()
     for f in sorted(os.listdir(os.path.join(ROOT, "quantized_kv_cache_08_gb300", "csrc"))):
-        with open(os.path.join(ROOT, "quantized_kv_cache_08_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "quantized_kv_cache_08_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(f.encode() + b"\0" + src.encode())
     return h.hexdigest()[:16]
 
 

@@ -73,7 +73,7 @@ typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype;
  *             low nibble << 4); codes round-half-away((x-m)/d) in [0,31]
  *             against the stored m and d                                24 B
  *   KVQ_FP8_E4M3: one byte per element, no scale (memra-engine "Module
- *             config", FP8-GLOBALS switch and kv_fp8_on: K/V held in e4m3).
+ *             cache", items gkv_on and kv_fp8_on: K/V held in e4m3).
  *             Read as OCP FP8 E4M3: sign, 4 exponent bits with bias 7, 3
  *             fraction bits, no infinities, largest finite 448; round to
  *             nearest, ties to even, magnitudes above 448 saturate to 448.

@@ -227,8 +227,8 @@ def q5_1_dequantize(blk) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # FP8 E4M3 (the alternative K/V format: one byte per element, no block scale)
 #
-# memra-engine "Module config", entries KV_FP8_FORCE, FP8-GLOBALS switch and
-# kv_fp8_on: K and V are held as e4m3 ("kf8vf8").  The pages name the format
+# memra-engine "Module cache", items KV_FP8_FORCE, gkv_on (the FP8-GLOBALS
+# switch) and kv_fp8_on: K and V are held as e4m3 ("kf8vf8").  The pages name the format
 # only; it is read as OCP FP8 E4M3: 1 sign bit, 4 exponent bits with bias 7,
 # 3 fraction bits, no infinities.  Normals are (1 + f/8) * 2**(E-7) for
 # E in 1..15 except E = 15, f = 7 (NaN); subnormals are f/8 * 2**-6; the

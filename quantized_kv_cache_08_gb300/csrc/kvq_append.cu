@@ -17,7 +17,7 @@
 // rounding boundary does it recompute the quotient in fp64 exactly as the
 // definition reads, so every code equals the fp64 decision.
 //
-// FP8 E4M3 (memra-engine "Module config", FP8-GLOBALS switch and kv_fp8_on:
+// FP8 E4M3 (memra-engine "Module cache", items gkv_on and kv_fp8_on:
 // K/V held in e4m3): each element becomes one byte on its own, with no scale,
 // by the hardware conversion that rounds to nearest even and saturates to
 // +-448 (cvt.rn.satfinite); byte e of a token row is element e.

@@ -32,7 +32,7 @@
 //            arithmetic and placed into the mantissa of 0.5 (value 0.5+u/256),
 //            so v_hat = 256 d * F + (m - 128 d) and o += (p*256d) F by packed
 //            FMAs, with sum p*(m - 128 d) kept per block.
-// FP8 E4M3 planes (memra-engine "Module config", kv_fp8_on: K/V held in e4m3)
+// FP8 E4M3 planes (memra-engine "Module cache", kv_fp8_on: K/V held in e4m3)
 // take the same phases with one byte per element and no block fields: a byte
 // moved into the sign, exponent and top fraction bits of a binary16 value is
 // the E4M3 value times 2^-8 (the exponent biases are 15 and 7, and subnormals
