@@ -43,7 +43,9 @@
  * Graph capture.  kvq_append, kvq_decode and kvq_truncate read the lengths and
  * the ring base on the device, so a captured append+decode step replays
  * correctly as the lengths grow.  After replaying a captured chain of appends
- * call kvq_note_replayed so the host mirror follows.  A ring rebase is decided
+ * call kvq_note_replayed so the host mirror follows; after one that contains
+ * kvq_truncate_device (its accepted counts read on the device), call
+ * kvq_sync_len instead.  A ring rebase is decided
  * on the host inside kvq_append: capture at most kvq_ring_headroom() appends.
  */
 #ifndef KVQ_H
@@ -180,13 +182,40 @@ kvq_status kvq_decode_noalloc(kvq_cache* cache, const void* q, kvq_dtype dtype, 
 
 /* Rollback ("Struct Cache", fn rollback, item C.1): set each sequence's
  * length to new_len[b] (a HOST array of n_seq values, usually
- * snapshot_len + accept_len), no data moves.  Needs new_len[b] <= len; a ring
+ * snapshot_len + accept_len), no data moves.  Needs new_len[b] <= len (the
+ * lower end while a kvq_truncate_device is pending); a ring
  * sequence also needs max(0, new_len + 1 - window) >= base (rewinds never
  * move the base), else KVQ_ERANGE. */
 kvq_status kvq_truncate(kvq_cache* cache, const int* new_len, void* stream);
 
+/* Rollback with the accepted counts on the device ("Struct Cache", fn
+ * rollback, item C.1, len = snapshot_len + accept_len, with snapshot_len =
+ * len - T for the T draft rows just appended and verified; "Struct KvLayer",
+ * field base_d: rewinds move len_d only).  accept_d: DEVICE int32 [n_seq],
+ * read when the kernel runs, so a captured graph replays with whatever it
+ * holds then.  For each sequence, len_d -= T - accept_d[b]: the first
+ * accept_d[b] of the last T rows stay.  The kernel checks 0 <= accept <= T,
+ * T <= len_d and, for a ring, max(0, new_len + 1 - window) >= base; a
+ * sequence that fails keeps its length and the device error word becomes 1.
+ * The host does not wait, so its mirror then knows each length only within
+ * [len - T, len]: appends check capacity against the upper end, a ring
+ * append that would rebase returns KVQ_ERANGE, decodes need T <= the lower
+ * end, and kvq_truncate takes only new_len <= the lower end (which makes the
+ * length exact again), until kvq_sync_len reads the lengths back.  The host
+ * refuses (KVQ_ERANGE, nothing enqueued) when a sequence may hold fewer than
+ * T rows or, for a ring, when accepting nothing would drop rows below base.
+ * After replaying a graph that contains this call, call kvq_sync_len before
+ * any other call on the cache (kvq_note_replayed cannot know the counts). */
+kvq_status kvq_truncate_device(kvq_cache* cache, const int* accept_d, int T, void* stream);
+
+/* Synchronise `stream` and read the device lengths into the host mirror,
+ * making it exact (after kvq_truncate_device).  KVQ_ERANGE if a device length
+ * lies outside its sequence's resident rows (the mirror is then unchanged). */
+kvq_status kvq_sync_len(kvq_cache* cache, void* stream);
+
 /* Host mirror of the lengths and ring bases (HOST arrays of n_seq ints;
- * either pointer may be NULL). */
+ * either pointer may be NULL).  After kvq_truncate_device and before
+ * kvq_sync_len the lengths are upper bounds. */
 kvq_status kvq_get_len(const kvq_cache* cache, int* len_host, int* base_host);
 
 /* Advance the host mirror after `steps` replays of a captured graph that

@@ -445,6 +445,19 @@ class OracleKvCache:
             self._k[b] = self._k[b][:n]
             self._v[b] = self._v[b][:n]
 
+    def rollback(self, accept, T):
+        """Rollback after a T-row draft step ("Struct Cache", fn rollback,
+        item C.1): len = snapshot_len + accept_len with snapshot_len = len - T,
+        so the first accept[b] of each sequence's last T rows stay."""
+        lens = self.lens()
+        new = []
+        for b, a in enumerate(accept):
+            a = int(a)
+            if not 0 <= a <= T or lens[b] < T:
+                raise ValueError("rollback: accept out of range")
+            new.append(lens[b] - T + a)
+        self.truncate(new)
+
     def rows(self, b, lo=0, hi=None):
         """Quantised bytes of logical rows [lo, hi) of sequence b."""
         return self._k[b][lo:hi], self._v[b][lo:hi]

@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ERANGE", 3: "KVQ_ECUDA", 4
 # every symbol include/kvq.h declares
 EXPORTS = (
     "kvq_required_bytes", "kvq_alloc", "kvq_free", "kvq_append", "kvq_decode",
-    "kvq_decode_noalloc", "kvq_truncate", "kvq_get_len", "kvq_note_replayed", "kvq_ring_headroom",
+    "kvq_decode_noalloc", "kvq_truncate", "kvq_truncate_device", "kvq_sync_len", "kvq_get_len", "kvq_note_replayed", "kvq_ring_headroom",
     "kvq_physical_rows", "kvq_read_device_error", "kvq_set_split_rows", "kvq_set_decode_path",
     "kvq_set_softcap",
     "kvq_block_bytes", "kvq_bytes_per_token", "kvq_last_error",
@@ -73,6 +73,8 @@ def lib():
             "kvq_decode": (I, [P, P, I, I, I, P, ctypes.c_float, P, P]),
             "kvq_decode_noalloc": (I, [P, P, I, I, I, P, ctypes.c_float, P, P]),
             "kvq_truncate": (I, [P, IP, P]),
+            "kvq_truncate_device": (I, [P, P, I, P]),
+            "kvq_sync_len": (I, [P, P]),
             "kvq_get_len": (I, [P, IP, IP]),
             "kvq_note_replayed": (I, [P, I, I]),
             "kvq_ring_headroom": (I, [P, I, IP]),
@@ -144,6 +146,14 @@ def kvq_decode_noalloc(handle, q, dtype, T, n_q_heads, sinks, scale, out, stream
 
 def kvq_truncate(handle, new_len, stream=0):
     _check(lib().kvq_truncate(handle, _ints(new_len), stream))
+
+
+def kvq_truncate_device(handle, accept_d, T, stream=0):
+    _check(lib().kvq_truncate_device(handle, accept_d, T, stream))
+
+
+def kvq_sync_len(handle, stream=0):
+    _check(lib().kvq_sync_len(handle, stream))
 
 
 def kvq_get_len(handle, n_seq):

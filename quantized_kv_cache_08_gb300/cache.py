@@ -107,6 +107,18 @@ class KVCache:
     def truncate(self, new_len, stream=None):
         B.kvq_truncate(self.handle, list(new_len), _stream_handle(stream))
 
+    def truncate_device(self, accept, T, stream=None):
+        """Keep the first accept[b] of each sequence's last T rows; accept is a
+        CUDA int32 tensor [n_seq] read when the kernel runs (no host wait)."""
+        _check_dev(accept, "accept")
+        if accept.dtype != torch.int32 or accept.numel() != self.n_seq:
+            raise ValueError("accept must be int32 [n_seq]")
+        B.kvq_truncate_device(self.handle, accept.data_ptr(), T, _stream_handle(stream))
+
+    def sync_len(self, stream=None):
+        """Wait for the stream and read the device lengths into the host mirror."""
+        B.kvq_sync_len(self.handle, _stream_handle(stream))
+
     # -- host-side helpers
     def lens(self):
         return B.kvq_get_len(self.handle, self.n_seq)[0]

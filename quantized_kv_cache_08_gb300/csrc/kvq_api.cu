@@ -37,6 +37,9 @@ struct kvq_cache {
     int fp8;                             // 1: K and V planes hold FP8 E4M3 bytes
     float softcap;                       // score cap (0: off)
     std::vector<int> len, base;
+    // lower bound of each length: equal to len except after kvq_truncate_device,
+    // when len_d lies in [len_lo, len] until kvq_sync_len or kvq_truncate
+    std::vector<int> len_lo;
 };
 
 namespace {
@@ -200,6 +203,7 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* 
     c->fp8 = g.fp8;
     c->softcap = 0.f;
     c->len.assign(cfg->n_seq, 0);
+    c->len_lo.assign(cfg->n_seq, 0);
     c->base.assign(cfg->n_seq, 0);
     e = cudaMemsetAsync(counters, 0, counters_bytes(cfg->n_seq), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
@@ -243,6 +247,10 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, kvq_dtype dtyp
         if (len + T - nb > c->rows) {
             if (!ring)
                 return fail(KVQ_ERANGE, "sequence %d: len %lld + T %d exceeds max_rows %d", b, len, T, c->rows);
+            if (c->len_lo[b] != c->len[b])
+                return fail(KVQ_ERANGE,
+                            "sequence %d: a ring rebase needs the exact length, pending a device-side rollback "
+                            "(call kvq_sync_len first)", b);
             nb = (int)(std::max(0LL, len + 1 - c->cfg.window) & ~31LL);
             if (len + T - nb > c->rows)
                 return fail(KVQ_ERANGE, "sequence %d: T %d does not fit the ring of %d rows", b, T, c->rows);
@@ -301,7 +309,10 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, kvq_dtype dtyp
         e = launch_commit(c->len_d, sid, T, s);
         if (e != cudaSuccess) return cuda_fail(e, "commit kernel");
     }
-    for (int b : ids) c->len[b] += T;
+    for (int b : ids) {
+        c->len[b] += T;
+        c->len_lo[b] += T;
+    }
     return KVQ_OK;
 }
 
@@ -336,7 +347,8 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
     long long total_vis = 0;
     for (int b = 0; b < B; ++b) {
-        if (c->len[b] < T) return fail(KVQ_ERANGE, "sequence %d holds %d rows, fewer than T=%d", b, c->len[b], T);
+        if (c->len_lo[b] < T)
+            return fail(KVQ_ERANGE, "sequence %d holds %d rows, fewer than T=%d", b, c->len_lo[b], T);
         total_vis += c->len[b] - vis_lo(c, c->len[b], T);
     }
     // rows per split: one wave of items for one sequence; otherwise about 5
@@ -494,8 +506,9 @@ kvq_status kvq_truncate(kvq_cache* c, const int* new_len, void* stream) {
     const int B = c->cfg.n_seq;
     for (int b = 0; b < B; ++b) {
         const int n = new_len[b];
-        if (n < 0 || n > c->len[b])
-            return fail(KVQ_ERANGE, "sequence %d: new length %d outside [0, %d]", b, n, c->len[b]);
+        if (n < 0 || n > c->len_lo[b])
+            return fail(KVQ_ERANGE, "sequence %d: new length %d outside [0, %d]%s", b, n, c->len_lo[b],
+                        c->len_lo[b] != c->len[b] ? " (a device-side rollback is pending: kvq_sync_len)" : "");
         if (c->cfg.ring && std::max(0, n + 1 - c->cfg.window) < c->base[b])
             return fail(KVQ_ERANGE, "sequence %d: rows below ring base %d are gone", b, c->base[b]);
     }
@@ -509,7 +522,43 @@ kvq_status kvq_truncate(kvq_cache* c, const int* new_len, void* stream) {
         cudaError_t e = launch_set_len(c->len_d, sid, new_len + first, s);
         if (e != cudaSuccess) return cuda_fail(e, "truncate kernel");
     }
-    for (int b = 0; b < B; ++b) c->len[b] = new_len[b];
+    for (int b = 0; b < B; ++b) c->len[b] = c->len_lo[b] = new_len[b];
+    return KVQ_OK;
+}
+
+kvq_status kvq_truncate_device(kvq_cache* c, const int* accept_d, int T, void* stream) {
+    if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+    if (!accept_d) return fail(KVQ_EINVAL, "accept_d is NULL");
+    if (T < 1 || T > c->cfg.max_t) return fail(KVQ_EINVAL, "T=%d outside [1, max_t=%d]", T, c->cfg.max_t);
+    const int B = c->cfg.n_seq;
+    for (int b = 0; b < B; ++b) {
+        if (c->len_lo[b] < T)
+            return fail(KVQ_ERANGE, "sequence %d may hold fewer than T=%d rows", b, T);
+        // the shortest outcome (nothing accepted) must keep its window resident
+        if (c->cfg.ring && std::max(0, c->len_lo[b] - T + 1 - c->cfg.window) < c->base[b])
+            return fail(KVQ_ERANGE, "sequence %d: rolling back T=%d rows would reach below ring base %d", b, T,
+                        c->base[b]);
+    }
+    cudaError_t e = launch_truncate_accept(c->len_d, c->base_d, c->err_d, accept_d, B, T, c->cfg.window,
+                                           c->cfg.ring, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "device-side truncate kernel");
+    for (int b = 0; b < B; ++b) c->len_lo[b] -= T;
+    return KVQ_OK;
+}
+
+kvq_status kvq_sync_len(kvq_cache* c, void* stream) {
+    if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+    const int B = c->cfg.n_seq;
+    std::vector<int> v(B);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaMemcpy(v.data(), c->len_d, sizeof(int) * (size_t)B, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read lengths");
+    for (int b = 0; b < B; ++b)
+        if (v[b] < c->base[b] || v[b] - c->base[b] > c->rows)
+            return fail(KVQ_ERANGE, "sequence %d: device length %d outside its resident rows", b, v[b]);
+    for (int b = 0; b < B; ++b) c->len[b] = c->len_lo[b] = v[b];
     return KVQ_OK;
 }
 
@@ -529,7 +578,10 @@ kvq_status kvq_note_replayed(kvq_cache* c, int steps, int T) {
     for (int b = 0; b < c->cfg.n_seq; ++b)
         if (c->len[b] + add - c->base[b] > c->rows)
             return fail(KVQ_ERANGE, "sequence %d would exceed its physical rows", b);
-    for (int b = 0; b < c->cfg.n_seq; ++b) c->len[b] += (int)add;
+    for (int b = 0; b < c->cfg.n_seq; ++b) {
+        c->len[b] += (int)add;
+        c->len_lo[b] += (int)add;
+    }
     return KVQ_OK;
 }
 

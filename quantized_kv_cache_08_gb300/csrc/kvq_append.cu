@@ -170,6 +170,27 @@ __global__ void set_len_kernel(int* len_d, SeqIds ids, SeqIds vals) {
 
 __global__ void set_base_kernel(int* base_d, int seq, int value) { base_d[seq] = value; }
 
+// Rollback with the accepted count on the device ("Struct Cache", fn rollback,
+// item C.1: len = snapshot_len + accept_len, where snapshot_len = len - T for
+// a T-row draft step): of the last T rows the first accept_d[b] stay.  A
+// sequence whose accept count is outside [0, T], that holds fewer than T rows,
+// or (ring) whose new window start would fall below its base keeps its length
+// and sets the error word.
+__global__ void truncate_accept_kernel(int* len_d, const int* base_d, int* err_d, const int* accept_d, int n,
+                                       int T, int window, int ring) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= n) return;
+    const int a = accept_d[b];
+    const int len = len_d[b];
+    const int nl = len - T + a;
+    bool ok = a >= 0 && a <= T && T <= len;
+    if (ok && ring) ok = max(0, nl + 1 - window) >= base_d[b];
+    if (ok)
+        len_d[b] = nl;
+    else
+        atomicExch(err_d, kErrCounter);
+}
+
 // Byte copy of two non-overlapping ranges (ring rebase legs, unaligned rows).
 __global__ void __launch_bounds__(256) ring_copy_bytes_kernel(const uint8_t* __restrict__ sk,
                                                              const uint8_t* __restrict__ sv,
@@ -237,6 +258,12 @@ cudaError_t launch_ring_copy(const uint8_t* src_k, const uint8_t* src_v, uint8_t
                                                      reinterpret_cast<const uint4*>(src_v),
                                                      reinterpret_cast<uint4*>(dst_k),
                                                      reinterpret_cast<uint4*>(dst_v), nk, nv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_truncate_accept(int* len_d, const int* base_d, int* err_d, const int* accept_d, int n, int T,
+                                   int window, int ring, cudaStream_t s) {
+    truncate_accept_kernel<<<(n + 255) / 256, 256, 0, s>>>(len_d, base_d, err_d, accept_d, n, T, window, ring);
     return cudaGetLastError();
 }
 

@@ -166,6 +166,9 @@ cudaError_t launch_set_len(int* len_d, const SeqIds& ids, const int* values, cud
 cudaError_t launch_ring_copy(const uint8_t* src_k, const uint8_t* src_v, uint8_t* dst_k,
                              uint8_t* dst_v, size_t k_bytes, size_t v_bytes, cudaStream_t s);
 cudaError_t launch_set_base(int* base_d, int seq, int value, cudaStream_t s);
+// len_d[b] -= T - accept_d[b] for b < n, checked on the device (error word on failure)
+cudaError_t launch_truncate_accept(int* len_d, const int* base_d, int* err_d, const int* accept_d, int n, int T,
+                                   int window, int ring, cudaStream_t s);
 
 // launchers (kvq_decode.cu)
 size_t split_smem_bytes(const SplitParams& p);

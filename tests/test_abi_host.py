@@ -121,5 +121,7 @@ def test_null_handle_calls(L):
     for fn, args in [(L.kvq_append, (None, 1, 1, 0, 1, None, 0, None)),
                      (L.kvq_decode, (None, 1, 0, 1, 8, None, 0.0, 1, None)),
                      (L.kvq_truncate, (None, None, None)),
+                     (L.kvq_truncate_device, (None, None, 1, None)),
+                     (L.kvq_sync_len, (None, None)),
                      (L.kvq_note_replayed, (None, 1, 1))]:
         assert fn(*args) == B.KVQ_EINVAL

@@ -541,3 +541,29 @@ def test_e4m3_cache_rows_and_attention_on_representable_values():
         ref = _sdpa_reference(q[b], k[b].astype(np.float64), v[b].astype(np.float64),
                               scale=1 / math.sqrt(D), sinks=sinks, window=0)
         np.testing.assert_allclose(got[b], ref, rtol=1e-11, atol=1e-11)
+
+
+def test_rollback_by_accept_count_equals_clean_build():
+    """After a T-row draft step, rollback(accept) leaves exactly the bytes of a
+    cache built from the snapshot rows plus the first accept draft rows."""
+    rng = np.random.default_rng(31)
+    n_kv, D, T = 2, 64, 6
+    snap = rng.standard_normal((2, 9, n_kv, D)).astype(np.float32)
+    draft = rng.standard_normal((2, T, n_kv, D)).astype(np.float32)
+    for fmt in ("q8_0/q5_1", "e4m3"):
+        c = O.OracleKvCache(2, n_kv, D, fmt=fmt)
+        c.append(snap, snap)
+        c.append(draft, -draft)
+        c.rollback([0, 4], T)
+        assert c.lens() == [9, 13]
+        clean = O.OracleKvCache(2, n_kv, D, fmt=fmt)
+        clean.append(snap, snap)
+        clean.append(draft[:, :4], -draft[:, :4], )
+        clean.truncate([9, 13])
+        for b in range(2):
+            for x, y in zip(c.rows(b), clean.rows(b)):
+                np.testing.assert_array_equal(x, y)
+        with pytest.raises(ValueError):
+            c.rollback([T + 1, 0], T)
+        with pytest.raises(ValueError):
+            c.rollback([-1, 0], T)
