@@ -81,14 +81,16 @@ def measured_peak():
 
 
 def kernel_source_hash():
-    """Hash of the CUDA sources with their comments removed, so that recorded
-    counters stay valid across comment-only edits and no longer."""
+    """Hash of the CUDA sources with comments removed and whitespace collapsed,
+    so that recorded counters stay valid across comment-only edits and no
+    longer."""
     h = hashlib.sha256()
     for f in sorted(os.listdir(os.path.join(ROOT, "quantized_kv_cache_08_gb300", "csrc"))):
         with open(os.path.join(ROOT, "quantized_kv_cache_08_gb300", "csrc", f)) as fh:
             src = fh.read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         src = re.sub(r"//[^\n]*", "", src)
+        src = " ".join(src.split())
         h.update(f.encode() + b"\0" + src.encode())
     return h.hexdigest()[:16]
 
