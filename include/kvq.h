@@ -224,7 +224,8 @@ kvq_status kvq_note_replayed(kvq_cache* cache, int steps, int T);
 
 /* Appends of T rows (to every sequence) that can run before a ring rebase is
  * due, i.e. how many steps a captured graph may replay. Flat caches: rows
- * left before max_rows, divided by T. */
+ * left before max_rows, divided by T.  While a kvq_truncate_device is
+ * pending it counts from the upper ends of the lengths (a safe undercount). */
 kvq_status kvq_ring_headroom(const kvq_cache* cache, int T, int* steps);
 
 /* fn physical_rows of "Struct KvLayer": map logical rows [start, end) of
