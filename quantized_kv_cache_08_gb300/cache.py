@@ -71,7 +71,7 @@ class KVCache:
             B.kvq_free(h)
             self.handle = None
 
-    # -- the four calls of the path
+    # -- the calls of the path: append, decode, truncate (host or device counts)
     def append(self, k, v, seq_ids=None, stream=None):
         """k, v: [n, T, Hkv, D] float32/bfloat16 CUDA tensors."""
         _check_dev(k, "k")
