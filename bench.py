@@ -18,7 +18,8 @@ the timed region.  `--impl reference` times the fp64 CPU oracle on a bounded
 sample of the same workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-       [--layers R] [--kv-format q8_0/q5_1|e4m3] [--impl kvq|reference]
+       [--layers R] [--kv-format q8_0/q5_1|e4m3] [--t T] [--softcap C]
+       [--impl kvq|reference]
 """
 
 from __future__ import annotations
@@ -93,6 +94,17 @@ def kernel_source_hash():
         src = " ".join(src.split())
         h.update(f.encode() + b"\0" + src.encode())
     return h.hexdigest()[:16]
+
+
+def traffic_key(name, fmt, args):
+    """Key of a run's recorded ncu traffic: the workload, plus every option
+    that changes the kernel or the shape (format, soft-capping, query rows)."""
+    key = name if fmt == "q8_0/q5_1" else f"{name}:{fmt}"
+    if args.softcap > 0:
+        key += ":softcap"
+    if args.t:
+        key += f":T{args.t}"
+    return key
 
 
 def recorded_traffic(name):
@@ -189,13 +201,18 @@ def barrier(world):
         dist.barrier()
 
 
+def bench_workload(args):
+    """The named workload, with its query rows per step overridden by --t."""
+    return workload(args.workload, **({"T": args.t} if args.t else {}))
+
+
 def run_kvq(args, world, rank, local):
     from quantized_kv_cache_08_gb300.cache import KVCache
 
     kbuild.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = workload(args.workload)
+    wl = bench_workload(args)
     T = wl.T
     lens = decode_lengths(wl)
     fmt = args.kv_format
@@ -220,6 +237,8 @@ def run_kvq(args, world, rank, local):
         else:
             c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=64, max_rows=max(lens),
                         window=wl.window, fmt=fmt)
+        if args.softcap > 0:
+            c.set_softcap(args.softcap)
         chunk = T if wl.ring else 64
         for b, L in enumerate(lens):
             k, v = wl.kv(b + 1000 * r + 100000 * rank, 0, L - T + 64 * T)
@@ -388,6 +407,8 @@ def run_kvq(args, world, rank, local):
         extra += f", window {wl.window}" + (f" over a ring of {caches[0].rows} rows" if wl.ring else "")
     if sinks is not None:
         extra += ", a sink logit per Q head"
+    if args.softcap > 0:
+        extra += f", scores soft-capped at {args.softcap:g}"
     cfg = {"workload": f"{wl.name}: {wl.n_seq} seq, {wl.n_q} Q / {wl.n_kv} KV heads, head_dim "
                        f"{wl.head_dim}, {sum(lens)} rows at decode, T={T}{extra}, q {wl.q_dtype}, "
                        f"{FORMATS[fmt][0]}",
@@ -407,7 +428,7 @@ def run_kvq(args, world, rank, local):
         "decode_ms_per_layer": round(dec_ms / decodes, 5),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(wl.name if fmt == "q8_0/q5_1" else f"{wl.name}:{fmt}"),
+                     "traffic": recorded_traffic(traffic_key(wl.name, fmt, args)),
                      "peak_source": peak_src,
                      "kernel": "kvq decode (split + merge)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -424,11 +445,11 @@ def run_kvq(args, world, rank, local):
         "clocks": clk,
     }
     if rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(wl, lens, sinks=sinks, fmt=fmt)
+        line["cpu_baseline"] = cpu_baseline(wl, lens, sinks=sinks, fmt=fmt, softcap=args.softcap)
     return line
 
 
-def cpu_baseline(wl, lens, budget_s=12.0, sinks=None, fmt="q8_0/q5_1"):
+def cpu_baseline(wl, lens, budget_s=12.0, sinks=None, fmt="q8_0/q5_1", softcap=0.0):
     """The fp64 oracle, as it stands, on a bounded sample of the workload: the
     decode of one layer for the first sequence (quantise its rows once, then
     dequantise + attend per repetition)."""
@@ -443,7 +464,7 @@ def cpu_baseline(wl, lens, budget_s=12.0, sinks=None, fmt="q8_0/q5_1"):
     reps, t_total = 0, 0.0
     while t_total < budget_s and reps < 20:
         t = time.perf_counter()
-        ora.decode(q, sinks=sk)
+        ora.decode(q, sinks=sk, softcap=softcap)
         t_total += time.perf_counter() - t
         reps += 1
     gbs = reps * visible_rows(wl, L) * kv_bytes_per_row(wl, fmt) / t_total / 1e9
@@ -456,15 +477,15 @@ def run_reference(args, world, rank):
     """The oracle as the reference arm: K timed steps, each a bounded sample."""
     if rank != 0:
         return None
-    wl = workload(args.workload)
+    wl = bench_workload(args)
     lens = decode_lengths(wl)
     base = cpu_baseline(wl, lens, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)),
-                        sinks=wl.sink_logits(), fmt=args.kv_format)
+                        sinks=wl.sink_logits(), fmt=args.kv_format, softcap=args.softcap)
     return {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "kv_format": args.kv_format,
-                                            "sample": base["sample"]},
+            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "kv_format": args.kv_format,
+                                            "softcap": args.softcap, "sample": base["sample"]},
             "cpu_baseline": base,
             "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -479,10 +500,18 @@ def main():
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--kv-format", default="q8_0/q5_1", choices=sorted(FORMATS),
                     help="K/V storage: q8_0 K with q5_1 V (default), or FP8 E4M3 K and V")
+    ap.add_argument("--t", type=int, default=0,
+                    help="query rows per step (appended, decoded causally, truncated); 0 = the workload's")
+    ap.add_argument("--softcap", type=float, default=0.0,
+                    help="score soft-capping c (s -> c tanh(s / c)); 0 = off")
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if not 0 <= args.t <= 64:
+        ap.error("--t must be in [1, 64] (0 = the workload's own)")
+    if args.softcap < 0:
+        ap.error("--softcap must be >= 0")
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         line = run_reference(args, world, rank)

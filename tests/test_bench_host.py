@@ -93,3 +93,22 @@ def test_formats_known_to_the_cache(fmt):
     from quantized_kv_cache_08_gb300.cache import KVCache
     assert fmt in KVCache.FORMATS
     assert KVCache.FORMATS[fmt][2] + KVCache.FORMATS[fmt][3] == bench.FORMATS[fmt][1]
+
+
+def test_traffic_key_separates_kernel_and_shape_options():
+    import argparse
+    a = argparse.Namespace(softcap=0.0, t=0)
+    assert bench.traffic_key("ctx32k", "q8_0/q5_1", a) == "ctx32k"
+    assert bench.traffic_key("ctx32k", "e4m3", a) == "ctx32k:e4m3"
+    assert bench.traffic_key("ctx32k", "q8_0/q5_1", argparse.Namespace(softcap=3.0, t=0)) == "ctx32k:softcap"
+    assert bench.traffic_key("swa_ring", "q8_0/q5_1", argparse.Namespace(softcap=0.0, t=8)) == "swa_ring:T8"
+
+
+def test_reference_arm_with_query_rows_and_softcap(capsys):
+    """--impl reference runs the oracle on CPU; --t and --softcap reach it."""
+    import argparse
+    args = argparse.Namespace(workload="ctx512", t=4, softcap=2.0, kv_format="q8_0/q5_1", steps=1,
+                              warmup=200)
+    line = bench.run_reference(args, 1, 0)
+    assert line["config"]["T"] == 4 and line["config"]["softcap"] == 2.0
+    assert line["value"] > 0 and "512 visible rows" in line["cpu_baseline"]["sample"]
