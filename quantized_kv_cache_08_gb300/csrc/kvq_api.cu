@@ -17,23 +17,23 @@ using namespace kvq;
 static constexpr int kMaxDevices = 64;
 
 struct kvq_cache {
-    CUtensorMap kmap, vmap;              // 3-D TMA maps of the planes (warp-specialised decode)
-    bool kmap_ok;
+    CUtensorMap kmap, vmap;              // 2-D TMA maps of the planes (stream-K decode)
+    bool smap_ok;
+    uint32_t Sk, Sv;                     // stream-K shared-memory row strides
     kvq_config cfg;
     uint8_t* k_plane;
     uint8_t* v_plane;
     int* len_d;
     int* base_d;
     int* err_d;
-    int* work_d;                         // decode work-item counter (0 between decodes)
     uint8_t* ws;
     size_t off_part_o, off_part_ml, off_plan, off_scratch;
     int kb, k_tok, v_tok, rows;          // rows = physical rows per sequence
     int max_vis;                         // most rows one decode may read per sequence
     int num_sms;
     int split_rows;                      // 0 = automatic
-    int path;                            // 0 auto, 1 generic split kernel, 2 warp-specialised
-    int nlimb;                           // query limbs of the warp-specialised kernel (2 or 3)
+    int path;                            // 0 auto, 1 generic split kernel, 2 stream-K kernel
+    int qbits;                           // query bits of the stream-K kernel (16 or 24)
     int fp8;                             // 1: K and V planes hold FP8 E4M3 bytes
     float softcap;                       // score cap (0: off)
     std::vector<int> len, base;
@@ -100,6 +100,35 @@ kvq_status check_config(const kvq_config* c, Geometry* g) {
     return KVQ_OK;
 }
 
+// Unit layout of the stream-K kernel for hpk Q heads per KV head and T query
+// rows: units of 4 queries, at most 16 per CTA (one per warp and row slice),
+// query slices for the rest, and rows of a tile split RS ways among the warps
+// of a unit.  ok = false when the geometry or format does not allow it.
+struct StreamShape {
+    bool ok;
+    int QPS, nqs, RS;
+};
+
+StreamShape stream_shape(const kvq_config* c, const Geometry& g, int hpk, int T) {
+    StreamShape sh{false, 1, 1, 1};
+    const int NBH = c->head_dim / 32;
+    if (g.fp8 || g.k_tok % 16 || g.v_tok % 16 || !(NBH == 2 || NBH == 4 || NBH == 8) || c->n_seq > kStreamMaxB ||
+        c->n_kv_heads > 16)
+        return sh;
+    const int nQG = (hpk * T + 3) / 4;
+    sh.QPS = std::max(1, std::min(nQG, 16 / c->n_kv_heads));
+    sh.nqs = (nQG + sh.QPS - 1) / sh.QPS;
+    const int nU = c->n_kv_heads * sh.QPS;
+    sh.RS = 2 * nU <= kStreamThreads / 32 ? 2 : 1;
+    sh.ok = (long long)sh.nqs * c->n_seq * g.rows < (1LL << 31);
+    return sh;
+}
+
+// Partial records of a stream-K decode on G CTAs
+size_t stream_records(const kvq_config* c, const StreamShape& sh, int G, int n_q_heads, int T) {
+    return ((size_t)G + (size_t)sh.nqs * c->n_seq) * (size_t)n_q_heads * T;
+}
+
 struct WsLayout {
     size_t part_o, part_ml, plan, scratch, total;
 };
@@ -107,11 +136,18 @@ struct WsLayout {
 WsLayout ws_layout(const kvq_config* c, const Geometry& g) {
     WsLayout w;
     const size_t items = (size_t)c->n_seq * ((g.max_vis + kMinSplitRows - 1) / kMinSplitRows);
-    const size_t recs = items * (size_t)c->max_q_heads * c->max_t;
+    size_t recs = items * (size_t)c->max_q_heads * c->max_t;
+    // the stream-K kernel's records for every (Q heads, T) a decode may pass
+    const int max_hpk = c->max_q_heads / c->n_kv_heads;
+    for (int hpk = 1; hpk <= max_hpk; ++hpk)
+        for (int T = 1; T <= c->max_t; ++T) {
+            const StreamShape sh = stream_shape(c, g, hpk, T);
+            if (sh.ok) recs = std::max(recs, stream_records(c, sh, kStreamMaxGrid, hpk * c->n_kv_heads, T));
+        }
     w.part_o = 0;
     w.part_ml = round_up(w.part_o + recs * c->head_dim * sizeof(float), 256);
     w.plan = round_up(w.part_ml + recs * 2 * sizeof(float), 256);
-    w.scratch = round_up(w.plan + (c->n_seq + 1) * sizeof(int), 256);
+    w.scratch = round_up(w.plan + (c->n_seq + 2 + kStreamMaxGrid) * sizeof(int), 256);
     w.total = w.scratch + (c->ring ? round_up((size_t)g.rows * (g.k_tok + g.v_tok), 256) : 0);
     return w;
 }
@@ -181,7 +217,6 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* 
     c->len_d = static_cast<int*>(counters);
     c->base_d = c->len_d + cfg->n_seq;
     c->err_d = c->base_d + cfg->n_seq;
-    c->work_d = c->err_d + 1;
     c->ws = static_cast<uint8_t*>(workspace);
     const WsLayout w = ws_layout(cfg, g);
     c->off_part_o = w.part_o;
@@ -195,11 +230,19 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* 
     c->max_vis = g.max_vis;
     c->num_sms = sms;
     c->split_rows = 0;
-    c->kmap_ok = g.k_tok % 16 == 0 && g.v_tok % 16 == 0 &&
-                 make_row_tensor_map(&c->kmap, k_plane, g.k_tok, (long long)cfg->n_seq * g.rows) &&
-                 make_row_tensor_map(&c->vmap, v_plane, g.v_tok, (long long)cfg->n_seq * g.rows);
+    // stream-K stage rows: K at an odd multiple of 16 bytes (consecutive rows
+    // in different bank groups), V at 64 mod 128 bytes
+    // (rows that are not 16-byte multiples cannot be tensor-copied at all)
+    const bool rows16 = g.k_tok % 16 == 0 && g.v_tok % 16 == 0;
+    c->Sk = (uint32_t)((g.k_tok / 16) % 2 ? g.k_tok : g.k_tok + 16);
+    c->Sv = (uint32_t)g.v_tok;
+    if (rows16)
+        c->Sv += (uint32_t)((64 - g.v_tok % 128 + 128) % 128);
+    c->smap_ok = !g.fp8 && rows16 &&
+                 make_stream_map(&c->kmap, k_plane, g.k_tok, (int)c->Sk, (long long)cfg->n_seq * g.rows) &&
+                 make_stream_map(&c->vmap, v_plane, g.v_tok, (int)c->Sv, (long long)cfg->n_seq * g.rows);
     c->path = 0;
-    c->nlimb = 2;                          // 16-bit queries unless 24 is asked for
+    c->qbits = 16;                         // 16-bit queries unless 24 is asked for
     c->fp8 = g.fp8;
     c->softcap = 0.f;
     c->len.assign(cfg->n_seq, 0);
@@ -332,29 +375,121 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     const int D = c->cfg.head_dim;
     const int hpk = n_q_heads / Hkv;
     const int Q = hpk * T;
-    const int QC = Q <= 4 ? 4 : 8;
-    const int NBH = D / 32;
-    const int nK = (QC / 4) * Hkv * NBH;
-    const bool generic_ok = 2 * nK <= kSplitThreads && kSplitThreads % (2 * nK) == 0;
-    // the warp-specialised kernel needs 16-byte token rows
-    // (value tasks per row: a power of two from 8 to 256, so each V warp holds
-    // a power-of-two number of tasks and its row groups reduce by butterfly)
-    // (no score cap: soft-capping runs on the generic kernel, so the
-    // warp-specialised kernel's hot loop carries no trace of it)
-    bool fast = c->path != 1 && !c->fp8 && c->kmap_ok && 2 * nK >= 8 && 2 * nK <= 256 && ((2 * nK) & (2 * nK - 1)) == 0 &&
-                Hkv <= 8 && c->softcap == 0.f;
-    if (!fast && !generic_ok)
-        return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
     long long total_vis = 0;
     for (int b = 0; b < B; ++b) {
         if (c->len_lo[b] < T)
             return fail(KVQ_ERANGE, "sequence %d holds %d rows, fewer than T=%d", b, c->len_lo[b], T);
         total_vis += c->len[b] - vis_lo(c, c->len[b], T);
     }
+    const float qscale = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
+    const float cap_a = c->softcap > 0.f ? 1.0f / (c->softcap * 1.4426950408889634f) : 0.f;
+    const float cap_b = c->softcap > 0.f ? c->softcap * 1.4426950408889634f : 0.f;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // ---- the stream-K kernel: q8_0 / q5_1, 16-byte token rows, head_dim 64, 128 or 256
+    Geometry g{c->kb, c->k_tok, c->v_tok, c->rows, c->max_vis, c->fp8};
+    const StreamShape sh = stream_shape(&c->cfg, g, hpk, T);
+    if (c->path != 1 && sh.ok && c->smap_ok) {
+        StreamParams p;
+        p.k_plane = c->k_plane;
+        p.v_plane = c->v_plane;
+        p.len_d = c->len_d;
+        p.base_d = c->base_d;
+        p.err_d = c->err_d;
+        p.q = q;
+        p.q_bf16 = dtype == KVQ_BF16;
+        p.qscale = qscale;
+        p.softcap_a = cap_a;
+        p.softcap_b = cap_b;
+        p.B = B;
+        p.T = T;
+        p.Hq = n_q_heads;
+        p.Hkv = Hkv;
+        p.hpk = hpk;
+        p.D = D;
+        p.k_tok = c->k_tok;
+        p.v_tok = c->v_tok;
+        p.max_rows = c->rows;
+        p.window = c->cfg.window;
+        p.Qh = Q;
+        p.QPS = sh.QPS;
+        p.nqs = sh.nqs;
+        p.RS = sh.RS;
+        p.NA = Hkv * sh.QPS * sh.RS;
+        p.Qtot = n_q_heads * T;
+        p.qbits = c->qbits;
+        p.Sk = c->Sk;
+        p.Sv = c->Sv;
+        // CTAs: one per SM, fewer when there are fewer 32-row tiles of work
+        const long long work = total_vis * sh.nqs;
+        p.G = (int)std::max(1LL, std::min<long long>((work + kStreamRows - 1) / kStreamRows,
+                                                     std::min(c->num_sms, kStreamMaxGrid)));
+        const int smem_max = stream_max_smem();
+        p.NS = 3;
+        while (p.NS > 2 && stream_layout(p).total > (size_t)smem_max) --p.NS;
+        if (stream_layout(p).total <= (size_t)smem_max) {
+            const size_t recs = stream_records(&c->cfg, sh, p.G, n_q_heads, T);
+            if (scratch) {
+                const size_t o_ml = round_up(recs * D * sizeof(float), 256);
+                const size_t o_plan = round_up(o_ml + recs * 2 * sizeof(float), 256);
+                const size_t need = o_plan + (B + 2 + p.G) * sizeof(int);
+                if (need > scratch_bytes)
+                    return fail(KVQ_ERANGE,
+                                "this decode needs %zu bytes of scratch, the no-alloc entry point holds %zu", need,
+                                scratch_bytes);
+                p.part_o = reinterpret_cast<float*>(scratch);
+                p.part_ml = reinterpret_cast<float*>(scratch + o_ml);
+                p.plan = reinterpret_cast<int*>(scratch + o_plan);
+            } else {
+                p.part_o = reinterpret_cast<float*>(c->ws + c->off_part_o);
+                p.part_ml = reinterpret_cast<float*>(c->ws + c->off_part_ml);
+                p.plan = reinterpret_cast<int*>(c->ws + c->off_plan);
+            }
+            cudaError_t e = launch_split_stream(p, c->kmap, c->vmap, s);
+            if (e != cudaSuccess) return cuda_fail(e, "decode split kernel");
+            MergeStreamParams m;
+            m.part_o = p.part_o;
+            m.part_ml = p.part_ml;
+            m.plan = p.plan;
+            m.sinks = sinks;
+            m.out = out;
+            m.B = B;
+            m.T = T;
+            m.Hq = n_q_heads;
+            m.hpk = hpk;
+            m.D = D;
+            m.Qtot = p.Qtot;
+            m.QPS = p.QPS;
+            m.nqs = p.nqs;
+            m.G = p.G;
+            // records per (sequence, query): RS per CTA whose range meets it;
+            // many records: 16 warps split them on 32-dim chunks, few: one
+            // warp per (sequence, query) over all dims
+            const long long keys = (long long)sh.nqs * B;
+            const long long recs_per = (p.G + keys - 1) / keys + 2;
+            int wpq = 1;
+            while (wpq < 16 && wpq * 16 < recs_per) wpq *= 2;
+            m.WPQ = wpq;
+            m.DC = wpq >= 4 ? 32 : std::min(D, 256);
+            e = launch_merge_stream(m, s);
+            if (e != cudaSuccess) return cuda_fail(e, "decode merge kernel");
+            return KVQ_OK;
+        }
+    }
+    if (c->path == 2)
+        return fail(KVQ_EUNSUPPORTED, c->fp8 ? "the stream-K decode reads q8_0/q5_1 only (use path 0 or 1)"
+                                             : "the stream-K decode does not support this geometry");
+
+    // ---- the generic split kernel
+    const int QC = Q <= 4 ? 4 : 8;
+    const int NBH = D / 32;
+    const int nK = (QC / 4) * Hkv * NBH;
+    const bool generic_ok = 2 * nK <= kSplitThreads && kSplitThreads % (2 * nK) == 0;
+    if (!generic_ok)
+        return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
     // rows per split: one wave of items for one sequence; otherwise about 5
-    // items per CTA in whole 32-row tiles (an item start costs a query
-    // preparation, a partial last tile costs nearly a full one; CTAs take
-    // items dynamically, so the tail costs about half an item)
+    // items per CTA (an item start costs a query preparation, a partial last
+    // tile costs nearly a full one)
     int C = c->split_rows;
     if (C == 0) {
         const long long per = B == 1 ? (total_vis + c->num_sms - 1) / c->num_sms
@@ -364,18 +499,16 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     const int max_splits = (c->max_vis + C - 1) / C;
 
     SplitParams p;
-    p.q_stage = 0;
     p.k_plane = c->k_plane;
     p.v_plane = c->v_plane;
     p.len_d = c->len_d;
     p.base_d = c->base_d;
     p.err_d = c->err_d;
-    p.work_d = c->work_d;
     p.q = q;
     p.q_bf16 = dtype == KVQ_BF16;
-    p.qscale = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
-    p.softcap_a = c->softcap > 0.f ? 1.0f / (c->softcap * 1.4426950408889634f) : 0.f;
-    p.softcap_b = c->softcap > 0.f ? c->softcap * 1.4426950408889634f : 0.f;
+    p.qscale = qscale;
+    p.softcap_a = cap_a;
+    p.softcap_b = cap_b;
     p.B = B;
     p.T = T;
     p.Hq = n_q_heads;
@@ -416,35 +549,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     const int smem_max = split_max_smem();
     p.nstage = 4;
     while (p.nstage > 2 && split_smem_bytes(p) > (size_t)smem_max) --p.nstage;
-    // warp-specialised layout: key rows at an odd multiple of 16 bytes, rings
-    // as deep as shared memory allows, row-group reduction in rounds of heads
-    p.nlimb = c->nlimb;
-    p.k_row_stride = (uint32_t)((c->k_tok / 16 + 1) % 2 ? c->k_tok + 16 : c->k_tok + 32);
-    p.k_boxes = (c->k_tok + 127) / 128;
-    p.v_boxes = (c->v_tok + 127) / 128;
-    if (fast) {
-        bool fits = false;
-        const int depths[4][2] = {{3, 3}, {3, 2}, {2, 3}, {2, 2}};
-        // stage next-item queries in shared memory when there is room and the
-        // query rows are 16-byte aligned
-        for (int stage_q = ((uintptr_t)q % 16 == 0) ? 1 : 0; stage_q >= 0 && !fits; --stage_q) {
-            p.q_stage = stage_q;
-            for (int di = 0; di < 4 && !fits; ++di) {
-                p.nstage_k = depths[di][0];
-                p.nstage_v = depths[di][1];
-                fits = fast_layout(p, p.nlimb).total <= (size_t)smem_max;
-            }
-        }
-        if (!fits) fast = false;
-    }
-    if (c->path == 2 && !fast)
-        return fail(KVQ_EUNSUPPORTED, c->fp8 ? "the warp-specialised decode reads q8_0/q5_1 only (use path 0 or 1)"
-                                      : c->softcap > 0.f
-                                          ? "the warp-specialised decode has no score cap (use path 0 or 1)"
-                                          : "the warp-specialised decode does not support this geometry");
-    if (!fast && !generic_ok)
-        return fail(KVQ_EUNSUPPORTED, "decode needs (queries/4) * n_kv_heads * head_dim/32 to divide 128");
-    if (!fast && split_smem_bytes(p) > (size_t)smem_max)
+    if (split_smem_bytes(p) > (size_t)smem_max)
         return fail(KVQ_EUNSUPPORTED, "decode tile does not fit shared memory (%zu bytes)", split_smem_bytes(p));
     long long items = 0;
     for (int b = 0; b < B; ++b) {
@@ -453,15 +558,13 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     }
     items *= p.nqs;
     const int grid = (int)std::max(1LL, std::min<long long>(items, c->num_sms));
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = fast ? launch_split_fast(p, c->kmap, c->vmap, grid, s) : launch_split(p, grid, s);
+    cudaError_t e = launch_split(p, grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode split kernel");
     MergeParams m;
     m.part_o = p.part_o;
     m.part_ml = p.part_ml;
     m.plan = p.plan;
     m.sinks = sinks;
-    m.work_d = c->work_d;
     m.out = out;
     m.B = B;
     m.Hq = n_q_heads;
@@ -635,7 +738,7 @@ kvq_status kvq_set_decode_path(kvq_cache* c, int path, int query_bits) {
     if (query_bits != 0 && query_bits != 16 && query_bits != 24)
         return fail(KVQ_EINVAL, "query_bits must be 0, 16 or 24");
     c->path = path;
-    c->nlimb = query_bits == 24 ? 3 : 2;
+    c->qbits = query_bits == 24 ? 24 : 16;
     return KVQ_OK;
 }
 

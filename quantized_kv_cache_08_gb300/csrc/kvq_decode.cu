@@ -567,8 +567,6 @@ __global__ void __launch_bounds__(merge_threads(VPL)) merge_kernel(const MergePa
     const int b = blockIdx.y;
     const int D = VPL * 32;
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // the split grid has completed: its work-item counter restarts at 0
-    if (p.work_d && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.work_d = 0;
     const bool live = gq < p.Qtot;
     const int first = p.plan[b];
     const int ns = live ? p.plan[b + 1] - first : 0;

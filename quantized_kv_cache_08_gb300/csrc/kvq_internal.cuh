@@ -20,9 +20,6 @@ constexpr int kSplitThreads = 256; // decode split CTA size
 constexpr int kTileRows = 16;      // KV rows staged per pipeline stage
 constexpr int kMinSplitRows = 64;  // smallest rows-per-split the workspace allows
 constexpr int kMergeThreads = 1024;
-constexpr int kFastThreads = 512;  // warp-specialised decode CTA size
-constexpr int kFastRows = 32;      // rows per tile of the warp-specialised decode
-constexpr int kFastPDepth = 4;     // probability buffers between its key and value warps
 
 // device error word codes
 constexpr int kErrCounter = 1;     // a length/base counter was out of range
@@ -55,7 +52,6 @@ struct SplitParams {
     const int* len_d;
     const int* base_d;
     int* err_d;
-    int* work_d;                   // work items handed out past the first wave (reset by the merge)
     const void* q;                 // [B][T][Hq][D]
     int q_bf16;
     float qscale;                  // score scale * log2(e)
@@ -72,18 +68,6 @@ struct SplitParams {
     int nstage;
     uint32_t k_stage_bytes;        // kTileRows * k_tok rounded to 128
     uint32_t stage_bytes;          // k + v stage bytes
-    // warp-specialised kernel only
-    int nstage_k, nstage_v;        // depths of the K and V stage rings
-    uint32_t k_row_stride;         // (generic layout only) stride of a staged key row
-    int k_boxes;                   // 128-byte column blocks per key row
-    int v_boxes;                   // 128-byte column blocks per value row
-    int nlimb;                     // int8 limbs per quantised query element (2 or 3)
-    int q_stage;                   // 1: stage the next item's queries in shared memory (cp.async)
-};
-
-// Shared-memory layout of the warp-specialised decode kernel (host and device).
-struct FastLayout {
-    size_t kstage, vstage, kring, vring, qlimb, qscale, qraw, P, alpha, qlo, qup, lens, bars, total;
 };
 
 __host__ __device__ inline size_t fl_round(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -115,46 +99,102 @@ inline cudaError_t kernel_attrs_once(F fn, std::atomic<unsigned long long>& done
     return cudaSuccess;
 }
 
-__host__ __device__ inline FastLayout fast_layout(const SplitParams& p, int nlimb) {
-    FastLayout L;
-    const size_t NQ = (size_t)p.Hkv * p.QC;
-    const size_t NBH = (size_t)p.D / 32;
-    // key tiles: k_boxes swizzled boxes of kFastRows x 128 bytes (1024-byte aligned)
-    L.kstage = (size_t)p.k_boxes * kFastRows * 128;
-    L.vstage = (size_t)p.v_boxes * kFastRows * 128;
+// Stream-K decode (kvq_decode_stream.cu): the visible rows of all sequences,
+// repeated once per query slice, form one work space cut into G equal
+// contiguous ranges, one per CTA; the part of a CTA's range inside one
+// (query slice, sequence) pair is a fragment, and fragment (c, key) writes its
+// partials to record slot c + key, key = slice * B + sequence.
+constexpr int kStreamThreads = 512;     // 16 warps, one (KV head, 4 queries) unit and row slice each
+constexpr int kStreamRows = 32;         // token rows per tile
+constexpr int kStreamMaxB = 1024;       // sequences the per-CTA tables hold
+constexpr int kStreamMaxGrid = 256;     // most CTAs a decode may use (record slots are sized by it)
+
+struct StreamParams {
+    const uint8_t* k_plane;
+    const uint8_t* v_plane;
+    const int* len_d;
+    const int* base_d;
+    int* err_d;
+    const void* q;                 // [B][T][Hq][D]
+    int q_bf16;
+    float qscale;                  // score scale * log2(e)
+    float softcap_a, softcap_b;    // score cap in log2 units: s -> b * tanh(a * s); b == 0: off
+    int B, T, Hq, Hkv, hpk, D, k_tok, v_tok, max_rows, window;
+    int Qh;                        // queries per KV head: hpk * T
+    int QPS;                       // query groups of 4 per KV head in one slice
+    int nqs;                       // query slices
+    int RS;                        // warps per unit (1 or 2): a tile's rows split RS ways
+    int NA;                        // working warps: Hkv * QPS * RS
+    int Qtot;                      // Hq * T
+    int G;                         // CTAs
+    int NS;                        // stages of each of the K and V rings
+    uint32_t Sk, Sv;               // shared-memory row strides of the K and V stages
+    int qbits;                     // 16 or 24: query quantisation
+    float* part_o;                 // [slot][Qtot][D]
+    float* part_ml;                // [slot][Qtot][2]  (max in log2 units, sum)
+    int* plan;                     // [B+1] prefix of visible rows, then [G+1] CTA range starts
+};
+
+struct StreamLayout {
+    size_t kst, vst, P, W, LW, SQ, CB, tabs, tinfo, bars, cnt, walk, total;
+    uint32_t kstage, vstage, pwarp, wwarp, lwarp;
+};
+
+__host__ __device__ inline StreamLayout stream_layout(const StreamParams& p) {
+    StreamLayout L;
+    const int warps = kStreamThreads / 32;
+    const int RW = kStreamRows / p.RS;
+    const int NBH = p.D / 32;
+    L.kstage = (uint32_t)kStreamRows * p.Sk;
+    L.vstage = (uint32_t)kStreamRows * p.Sv;
+    L.pwarp = (uint32_t)RW * 16;                    // [RW rows][4 queries] f32
+    L.wwarp = (uint32_t)NBH * 256;                  // [block][8 pairs of pairs][4 queries][2] 16-bit pairs
+    L.lwarp = p.qbits == 24 ? (uint32_t)NBH * 9 * 16 : 0u;   // [block][9 words][4 queries] low bytes
     size_t off = 0;
-    L.kring = off;
-    off += (size_t)p.nstage_k * L.kstage;
-    L.vring = off;
-    off += (size_t)p.nstage_v * L.vstage;
-    L.qlimb = off;
-    off += fl_round(NQ * p.D * nlimb, 16);
-    L.qscale = off;
-    off += fl_round(NQ * NBH * 4, 16);
-    L.qraw = off;                  // next item's raw queries [NQ][D] (bf16 or f32)
-    off += p.q_stage ? fl_round(NQ * p.D * (p.q_bf16 ? 2 : 4), 16) : 0;
+    L.kst = off;
+    off += (size_t)p.NS * L.kstage;
+    L.vst = off;
+    off += (size_t)p.NS * L.vstage;
     L.P = off;
-    off += fl_round((size_t)kFastPDepth * kFastRows * (NQ + 4) * 4, 16);
-    L.alpha = off;
-    off += fl_round((size_t)kFastPDepth * NQ * 4, 16);
-    L.qlo = off;
-    off += fl_round(NQ * 4, 16);
-    L.qup = off;
-    off += fl_round(NQ * 4, 16);
-    L.lens = off;
-    off += fl_round((3 * (size_t)p.B + 1) * 4, 16);
+    off += (size_t)warps * L.pwarp;
+    L.W = off;
+    off += (size_t)warps * L.wwarp;
+    L.LW = off;
+    off += (size_t)warps * L.lwarp;
+    L.SQ = off;
+    off += (size_t)warps * 64;
+    L.CB = off;                                     // two row slices: per unit [4][D] sums + 8 floats
+    off += p.RS == 2 ? (size_t)(warps / 2) * (16 * (size_t)p.D + 32) : 0;
+    L.tabs = off;                                   // len, base, lo, vis, prefix: 5 x (B + 1) ints
+    off += fl_round((size_t)5 * (p.B + 1) * 4, 16);
+    L.tinfo = off;
+    off += (size_t)2 * p.NS * 16;
     L.bars = off;
-    off += 8 * (size_t)(p.nstage_k + p.nstage_v);
-    L.total = off + 1024;          // slack to align the base to 1024 bytes
+    off += (size_t)2 * p.NS * 8;
+    L.cnt = off;                                    // release counters and armed-phase counts
+    off += fl_round((size_t)4 * p.NS * 4, 16);
+    L.walk = off;
+    off += 64;
+    L.total = off + 128;                            // slack to align the base to 128 bytes
     return L;
 }
+
+struct MergeStreamParams {
+    const float* part_o;
+    const float* part_ml;
+    const int* plan;               // [B+1] prefix of visible rows, [G+1] CTA range starts
+    const float* sinks;            // [Hq] or null
+    float* out;                    // [B][T][Hq][D]
+    int B, T, Hq, hpk, D, Qtot, QPS, nqs, G;
+    int WPQ;                       // warps per (sequence, query, dim chunk)
+    int DC;                        // dims per chunk (32 * dims per lane)
+};
 
 struct MergeParams {
     const float* part_o;
     const float* part_ml;
     const int* plan;               // [B+1]
     const float* sinks;            // [Hq] or null
-    int* work_d;                   // the split kernel's work-item counter, reset here
     float* out;                    // [B][T][Hq][D]
     int B, Hq, Qtot, D;
 };
@@ -174,12 +214,16 @@ cudaError_t launch_truncate_accept(int* len_d, const int* base_d, int* err_d, co
 size_t split_smem_bytes(const SplitParams& p);
 int split_max_smem();
 cudaError_t launch_split(const SplitParams& p, int grid, cudaStream_t s);
-// warp-specialised decode (kvq_decode_fast.cu): token rows must be 16-byte multiples
-cudaError_t launch_split_fast(const SplitParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
-                              cudaStream_t s);
-// 3-D TMA map of a byte plane of `rows` token rows: one box = kFastRows rows x
-// all 128-byte column blocks, 128-byte swizzle
-bool make_row_tensor_map(CUtensorMap* map, void* plane, int tok_bytes, long long rows);
 cudaError_t launch_merge(const MergeParams& p, int T, int max_splits, bool pdl, cudaStream_t s);
+
+// stream-K decode (kvq_decode_stream.cu): token rows must be 16-byte multiples
+cudaError_t launch_split_stream(const StreamParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                cudaStream_t s);
+// 2-D TMA map of a byte plane of `rows` token rows of tok_bytes (a multiple of
+// 16) as 8-byte elements, box = 32 rows of stride_bytes (>= tok_bytes, a
+// multiple of 16, at most 2048): the box part past a token row is zero-filled
+bool make_stream_map(CUtensorMap* map, void* plane, int tok_bytes, int stride_bytes, long long rows);
+cudaError_t launch_merge_stream(const MergeStreamParams& p, cudaStream_t s);
+int stream_max_smem();
 
 }  // namespace kvq

@@ -10,13 +10,13 @@ import torch
 
 from quantized_kv_cache_08_gb300 import _binding as B
 from quantized_kv_cache_08_gb300.cache import KVCache, _dtype_code
+from tests.kvq_testutil import need_gpu
 
 pytestmark = pytest.mark.gpu
 
 
 def _need_gpu():
-    if not torch.cuda.is_available():
-        pytest.skip("needs a CUDA device")
+    need_gpu()      # raises without a GPU: there is no CPU fallback to test
 
 
 def _noalloc(cache, q, sinks=None, scale=0.0):
@@ -38,7 +38,7 @@ def _filled(n_seq, Hkv, D, Hq, lens, seed, **kw):
     return c, g
 
 
-@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("path", [0, 1, 2])
 @pytest.mark.parametrize("shape", [
     # n_seq, Hkv, D, Hq, lens, T, sinks, q dtype
     (1, 8, 128, 32, [4096], 1, False, torch.bfloat16),
@@ -68,6 +68,7 @@ def test_noalloc_refuses_oversize_partials():
     # 64-row splits over 32768 rows: 512 splits x 64 queries x (128 + 2)
     # floats is about 17 MB, above the 16 MiB scratch
     c = KVCache(1, 8, 128, 64, max_t=1, max_rows=32768)
+    c.set_decode_path(1)
     c.set_split_rows(64)
     k = torch.randn(1, 1, 8, 128, device="cuda")
     c.append(k, k)
