@@ -93,14 +93,14 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // Bounded wait; false once any wait of the CTA has run out (error word set).
-// The clock and the abort flag are read once per 16 tries.
+// A waiting warp sleeps in try_wait (up to 20 us a try) instead of spinning,
+// so it takes no issue slots from the warps still working; the clock and the
+// abort flag are read between tries.
 __device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err_d) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 16; ++i)
-            if (mbar_try(bar, parity)) return true;
+        if (mbar_try_sleep(bar, parity, 20000u)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitCycles) {
             atomicExch(err_d, kErrWait);
@@ -795,10 +795,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StreamParams 
                 for (int o = VH; o < 32; o <<= 1) {
                     pm[n] += __shfl_xor_sync(0xffffffffu, pm[n], o);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        o2[n][c].x += __shfl_xor_sync(0xffffffffu, o2[n][c].x, o);
-                        o2[n][c].y += __shfl_xor_sync(0xffffffffu, o2[n][c].y, o);
-                    }
+                    for (int c = 0; c < 8; ++c)
+                        o2[n][c] = __fadd2_rn(o2[n][c], make_float2(__shfl_xor_sync(0xffffffffu, o2[n][c].x, o),
+                                                                    __shfl_xor_sync(0xffffffffu, o2[n][c].y, o)));
                 }
                 // o = sum 256 p d F + sum 256 p (m - 128 d) / 256
                 const float a = pm[n] * (1.f / 256.f);
@@ -920,7 +919,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StreamParams 
 //   out = sum o_r 2^(m_r - M) / L.
 // The records of (b, q) are those of the CTAs whose ranges meet the rows
 // [xa, xb) of key (slice of q, b): CTA c covers [c W / G, (c + 1) W / G), so
-// the CTA holding row x is ((x + 1) G - 1) / W.  A CTA has 16 warps; WPQ
+// the CTA holding row x is ((x + 1) G - 1) / W; the split kernel also writes
+// the range starts, which tell an empty range (no record) apart.  A CTA has 16 warps; WPQ
 // warps share one (sequence, query, chunk of DC = 32 * VPL dims), each
 // folding every WPQ-th record with U records' loads in flight, and their
 // states meet in shared memory.
@@ -953,21 +953,12 @@ __global__ void __launch_bounds__(kThreads) merge_stream_kernel(const MergeStrea
     const int xb = xa + (p.plan[b + 1] - p.plan[b]);
     int c_lo = 0, nrec = 0;
     if (live && xb > xa) {
-        // the CTAs holding rows xa and xb - 1: the last c with starts[c] <= x
-        int lo = 0, hi = p.G;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (starts[mid] <= xa) lo = mid;
-            else hi = mid;
-        }
-        c_lo = lo;
-        hi = p.G;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (starts[mid] <= xb - 1) lo = mid;
-            else hi = mid;
-        }
-        nrec = lo - c_lo + 1;
+        // the CTAs holding rows xa and xb - 1: CTA c starts at floor(c W / G),
+        // so the CTA of row x is ((x + 1) G - 1) / W
+        const long long W = (long long)R * p.nqs;
+        c_lo = (int)(((long long)(xa + 1) * p.G - 1) / W);
+        const int c_hi = (int)(((long long)xb * p.G - 1) / W);
+        nrec = c_hi - c_lo + 1;
     }
     const int dim0 = ch * DC + lane * VPL;
     float M = kNegInf, Ls = 0.f, acc[VPL];
