@@ -18,8 +18,12 @@ the timed region.  `--impl reference` times the fp64 CPU oracle on a bounded
 sample of the same workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-       [--layers R] [--kv-format q8_0/q5_1|e4m3] [--t T] [--softcap C]
-       [--impl kvq|reference]
+       [--also NAME,...|none] [--layers R] [--kv-format q8_0/q5_1|e4m3] [--t T]
+       [--softcap C] [--rollback host|device] [--impl kvq|reference]
+
+The headline line is --workload (ctx32k by default); the workloads named by
+--also (batch64 by default) are measured in the same run and reported under
+"workloads", each with its own value, roofline, e2e and CPU baseline.
 """
 
 from __future__ import annotations
@@ -206,13 +210,17 @@ def bench_workload(args):
     return workload(args.workload, **({"T": args.t} if args.t else {}))
 
 
-def run_kvq(args, world, rank, local):
+DTYPE = ("k.q: int16 queries x int8 codes (dp2a, int32 sums, f32 per block); "
+         "p.v: f32 (packed FMA)")
+
+
+def measure(args, name, world, rank, local):
+    """One workload: build R layer caches, time the captured step, return the
+    workload's result (value, roofline, e2e, clocks, config)."""
     from quantized_kv_cache_08_gb300.cache import KVCache
 
-    kbuild.build()
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = bench_workload(args)
+    wl = workload(name, **({"T": args.t} if args.t else {}))
     T = wl.T
     lens = decode_lengths(wl)
     fmt = args.kv_format
@@ -226,6 +234,10 @@ def run_kvq(args, world, rank, local):
     sinks = wl.sink_logits()
     sinks_d = None if sinks is None else sinks.to(dev)
     scratch = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    device_rollback = args.rollback == "device"
+    # rows past the step's length: the e2e legs run their steps before the
+    # host mirror is read back (device rollback), each step appending T rows
+    spare = T * (4 * (args.steps + args.warmup) + 8) if device_rollback else T
 
     # --- build R layer caches holding len-T rows each (prefill, untimed);
     # a ring fills with T-row steps, a flat cache with 64-row chunks
@@ -235,7 +247,7 @@ def run_kvq(args, world, rank, local):
             c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=T, window=wl.window, ring=True,
                         fmt=fmt)
         else:
-            c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=64, max_rows=max(lens),
+            c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=max(64, T), max_rows=max(lens) + spare,
                         window=wl.window, fmt=fmt)
         if args.softcap > 0:
             c.set_softcap(args.softcap)
@@ -268,6 +280,15 @@ def run_kvq(args, world, rank, local):
         qs.append(wl.q(r + 7 * rank, T=T).to(dev))
     outs = [torch.empty(wl.n_seq, T, wl.n_q, wl.head_dim, dtype=torch.float32, device=dev)
             for _ in range(R)]
+    accept0 = torch.zeros(wl.n_seq, dtype=torch.int32, device=dev)
+
+    def rollback(c):
+        """Back to the snapshot: T draft rows, none accepted."""
+        if device_rollback:
+            c.truncate_device(accept0, T)
+        else:
+            c.truncate(base_len)
+
     torch.cuda.synchronize()
 
     def step(events=None, decode=True):
@@ -281,7 +302,13 @@ def run_kvq(args, world, rank, local):
                 c.decode(qs[r], sinks=sinks_d, out=outs[r])
             if events is not None:
                 events[r][1].record(stream)
-            c.truncate(base_len)
+            rollback(c)
+
+    def sync_all():
+        torch.cuda.synchronize()
+        if device_rollback:
+            for c in caches:
+                c.sync_len()
 
     def capture(fn):
         g = torch.cuda.CUDAGraph()
@@ -300,7 +327,7 @@ def run_kvq(args, world, rank, local):
         return a.elapsed_time(b)
 
     # eager warm-up (kernel attributes, lazy module loads), then capture.  The
-    # counters live on the device, so the captured append / decode / truncate
+    # counters live on the device, so the captured append / decode / rollback
     # replay with the right lengths.  The decode time is what the decode adds
     # to the step: the K-step graph (the timed region) minus the same graph
     # without the decodes, both timed by CUDA events around the replay on the
@@ -308,7 +335,7 @@ def run_kvq(args, world, rank, local):
     # so the per-decode event brackets and a graph of back-to-back decodes are
     # reported beside it as cross-checks only.
     step()
-    torch.cuda.synchronize()
+    sync_all()
     g_warm = capture(step)
     g_timed = capture(lambda: [step() for _ in range(args.steps)])
     g_nodec = capture(lambda: [step(decode=False) for _ in range(args.steps)])
@@ -324,7 +351,7 @@ def run_kvq(args, world, rank, local):
             for r, c in enumerate(caches):
                 c.decode(qs[r], sinks=sinks_d, out=outs[r])
     g_dec = capture(dec_only)
-    torch.cuda.synchronize()
+    sync_all()
     for _ in range(args.warmup):
         g_warm.replay()
     torch.cuda.synchronize()
@@ -347,6 +374,7 @@ def run_kvq(args, world, rank, local):
     dec_ms = max_over_ranks(step_ms - nodec_ms, world)
     timing = ("decode = CUDA-graph replay of K steps minus the same K steps without the decode, "
               "CUDA events around each replay on the launching stream")
+    sync_all()
     for c in caches:
         if c.device_error() != 0:
             raise SystemExit("device error word set during the benchmark")
@@ -358,29 +386,35 @@ def run_kvq(args, world, rank, local):
     achieved = kv_bytes_step * args.steps / (dec_ms * 1e-3) / 1e9  # per GPU
     peak, peak_src = measured_peak()
 
-    # --- end to end through the public API: pinned host inputs in, output out
-    pin_k = [x.cpu().pin_memory() for x in k_new]
-    pin_v = [x.cpu().pin_memory() for x in v_new]
-    pin_q = [x.cpu().pin_memory() for x in qs]
+    # --- end to end through the public API: the step's inputs (K, V rows and
+    # queries, in their own dtypes) in one pinned host buffer copied in with
+    # one copy, every output copied out
+    segs, off = [], 0
+    for x in k_new + v_new + qs:
+        nb = x.numel() * x.element_size()
+        segs.append((off, nb, x))
+        off += (nb + 255) // 256 * 256
+    host_in = torch.empty(off, dtype=torch.uint8).pin_memory()
+    dev_in = torch.empty(off, dtype=torch.uint8, device=dev)
+    ins = []
+    for o, nb, x in segs:
+        host_in[o:o + nb].copy_(x.reshape(-1).view(torch.uint8).cpu())
+        ins.append(dev_in[o:o + nb].view(x.dtype).view(x.shape))
+    dk, dv, dq = ins[:R], ins[R:2 * R], ins[2 * R:]
     pin_o = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    dk = [torch.empty_like(x) for x in k_new]
-    dv = [torch.empty_like(x) for x in v_new]
-    dq = [torch.empty_like(x) for x in qs]
 
     def e2e_step():
+        dev_in.copy_(host_in, non_blocking=True)
         for r, c in enumerate(caches):
-            dk[r].copy_(pin_k[r], non_blocking=True)
-            dv[r].copy_(pin_v[r], non_blocking=True)
-            dq[r].copy_(pin_q[r], non_blocking=True)
             c.append(dk[r], dv[r])
             c.decode(dq[r], sinks=sinks_d, out=outs[r])
             pin_o[r].copy_(outs[r], non_blocking=True)
-            c.truncate(base_len)
+            rollback(c)
 
     # eager: every call from Python, as a caller without graphs makes them
     for _ in range(args.warmup):
         e2e_step()
-    torch.cuda.synchronize()
+    sync_all()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -390,15 +424,17 @@ def run_kvq(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_eager_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    sync_all()
     # captured: the same public calls and copies (pinned host -> device inputs,
     # device -> pinned host outputs) replayed as one CUDA graph of K steps
     g_e2e = capture(lambda: [e2e_step() for _ in range(args.steps)])
     for _ in range(args.warmup):
         g_e2e.replay()
-    torch.cuda.synchronize()
+    sync_all()
     barrier(world)
     e2e_ms = max_over_ranks(statistics.median(replay_ms(g_e2e) for _ in range(3)), world)
-    h2d = sum(x.numel() * x.element_size() for x in pin_k + pin_v + pin_q)
+    sync_all()
+    h2d = sum(nb for _, nb, _ in segs)
     d2h = sum(x.numel() * x.element_size() for x in pin_o)
     e2e_value = world * kv_bytes_step * args.steps / (e2e_ms * 1e-3) / 1e9
 
@@ -414,16 +450,15 @@ def run_kvq(args, world, rank, local):
                        f"{FORMATS[fmt][0]}",
            "layers": R, "rows_total": sum(lens), "rows_visible": sum(vis),
            "kv_bytes_per_decode": footprint,
-           "step": f"per layer: append {T} row(s) + decode + truncate back",
+           "step": (f"per layer: append {T} row(s) + decode + rollback to the snapshot "
+                    f"({'device-side accepted counts' if device_rollback else 'host lengths'})"),
            "l2": (f"L2 flushed every step ({2 * L2_BYTES // 2**20} MiB write), {R} layer caches"
                   if flush else
                   f"inputs larger than L2: {R} layer caches, {R * footprint / 1e6:.0f} MB rotated")}
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
+    res = {
+        "value": round(value, 2), "unit": "GB/s",
         "ms_per_step": round(total_ms / args.steps, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": cfg,
+        "config": cfg,
         "tokens_per_s": round(tokens_per_s, 1),
         "decode_ms_per_layer": round(dec_ms / decodes, 5),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
@@ -433,19 +468,71 @@ def run_kvq(args, world, rank, local):
                      "kernel": "kvq decode (split + merge)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4),
-                "how": "K steps of the public calls with their pinned-host copies, captured as one "
-                       "CUDA graph and replayed; the whole step's time (append, decode, truncate, "
-                       "copies) divides the decode's bytes",
+                "how": "K steps of the public calls with their pinned-host copies (the step's K, V "
+                       "and queries in one buffer, each output back), captured as one CUDA graph and "
+                       "replayed; the whole step's time (copies, append, decode, rollback) divides the "
+                       "decode's bytes",
                 "eager_value": round(world * kv_bytes_step * args.steps / (e2e_eager_ms * 1e-3) / 1e9, 2)},
-        "gpu_launches": 5 * R * args.steps,
+        # append, split, merge, rollback per layer and step
+        "gpu_launches": 4 * R * args.steps,
         "timing": timing,
         "decode_only_ms_per_layer": round(dec_only_ms / decodes, 5),
         "decode_event_bracket_ms_per_layer": None if bracket_ms is None else round(bracket_ms / decodes, 5),
         "step_without_decode_ms_per_layer": round(nodec_ms / decodes, 5),
         "clocks": clk,
     }
+    if wl.ring:
+        res["ring_growth"] = ring_growth(caches[0], wl, k_new[0], v_new[0], qs[0], sinks_d, outs[0],
+                                         args, row_bytes, vis[0], world)
     if rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(wl, lens, sinks=sinks, fmt=fmt, softcap=args.softcap)
+        res["cpu_baseline"] = cpu_baseline(wl, lens, sinks=sinks, fmt=fmt, softcap=args.softcap)
+    del caches, g_warm, g_timed, g_nodec, g_ev, g_dec, g_e2e
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def ring_growth(c, wl, k1, v1, q1, sinks_d, out, args, row_bytes, vis, world, steps=256):
+    """A ring that keeps growing: eager append + decode steps with no rollback,
+    so every 32nd append rebases the ring (moves the live window to row 0)
+    inside the timed region; CUDA events around the K steps."""
+    T = wl.T
+    for _ in range(8):
+        c.append(k1, v1)
+        c.decode(q1, sinks=sinks_d, out=out)
+    torch.cuda.synchronize()
+    b0 = c.bases()[0]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        c.append(k1, v1)
+        c.decode(q1, sinks=sinks_d, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    rebases = (c.bases()[0] - b0) // 32
+    return {"steps": steps, "ms_per_step": round(ms / steps, 5),
+            "rebases": int(rebases),
+            "value": round(world * vis * row_bytes * steps / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "how": f"eager append of {T} row(s) + decode per step, the length growing (no rollback), a ring "
+                   "rebase every 32 appends inside the timed region; the decode's bytes over the whole step"}
+
+
+def run_kvq(args, world, rank, local):
+    kbuild.build()
+    torch.cuda.set_device(local)
+    res = measure(args, args.workload, world, rank, local)
+    line = {"metric": METRIC, "value": res.pop("value"), "unit": res.pop("unit"), "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
+            "data": "synthetic"}
+    line.update(res)
+    extras = [w for w in (args.also.split(",") if args.also and args.also != "none" else [])
+              if w and w != args.workload]
+    if extras:
+        line["workloads"] = {w: measure(args, w, world, rank, local) for w in extras}
+        line["gpu_launches"] += sum(v["gpu_launches"] for v in line["workloads"].values())
     return line
 
 
@@ -504,12 +591,18 @@ def main():
                     help="query rows per step (appended, decoded causally, truncated); 0 = the workload's")
     ap.add_argument("--softcap", type=float, default=0.0,
                     help="score soft-capping c (s -> c tanh(s / c)); 0 = off")
+    ap.add_argument("--also", default="batch64",
+                    help="comma-separated workloads measured in the same run, reported under "
+                         "'workloads' (none: only --workload)")
+    ap.add_argument("--rollback", default="host", choices=["host", "device"],
+                    help="how each step rolls back to the snapshot: host lengths (kvq_truncate) or "
+                         "accepted counts on the device (kvq_truncate_device)")
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if not 0 <= args.t <= 64:
-        ap.error("--t must be in [1, 64] (0 = the workload's own)")
+    if not 0 <= args.t <= 512:
+        ap.error("--t must be in [1, 512] (0 = the workload's own)")
     if args.softcap < 0:
         ap.error("--softcap must be >= 0")
     world, rank, local = dist_setup(args)

@@ -88,7 +88,7 @@ typedef struct kvq_config {
     int n_kv_heads;   /* Hkv                                                       */
     int head_dim;     /* D: multiple of 32, at most 512                            */
     int max_q_heads;  /* largest Hq a decode may pass (a multiple of Hkv)          */
-    int max_t;        /* largest T of one append or decode call (1..64)            */
+    int max_t;        /* largest T of one append or decode call (1..512)           */
     int max_rows;     /* physical rows per sequence.  Flat cache: the logical      */
                       /* capacity.  Ring: 0 selects window + 30 + max_t.           */
     int window;       /* 0: full attention; > 0: each query row sees at most the   */

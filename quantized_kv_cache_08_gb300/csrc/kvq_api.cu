@@ -77,7 +77,7 @@ kvq_status check_config(const kvq_config* c, Geometry* g) {
         return fail(KVQ_EINVAL, "head_dim must be a multiple of 32 in [32, 512] (a block never straddles a head)");
     if (c->max_q_heads < c->n_kv_heads || c->max_q_heads % c->n_kv_heads)
         return fail(KVQ_EINVAL, "max_q_heads must be a positive multiple of n_kv_heads");
-    if (c->max_t < 1 || c->max_t > 64) return fail(KVQ_EINVAL, "max_t must be in [1, 64]");
+    if (c->max_t < 1 || c->max_t > 512) return fail(KVQ_EINVAL, "max_t must be in [1, 512]");
     if (c->window < 0) return fail(KVQ_EINVAL, "window must be >= 0");
     if (c->ring && c->window <= 0) return fail(KVQ_EINVAL, "a ring cache needs window > 0");
     const long long kvd = (long long)c->n_kv_heads * c->head_dim;
@@ -125,8 +125,8 @@ StreamShape stream_shape(const kvq_config* c, const Geometry& g, int hpk, int T)
 }
 
 // Partial records of a stream-K decode on G CTAs
-size_t stream_records(const kvq_config* c, const StreamShape& sh, int G, int n_q_heads, int T) {
-    return ((size_t)G + (size_t)sh.nqs * c->n_seq) * (size_t)n_q_heads * T;
+size_t stream_records(const kvq_config* c, const StreamShape& sh, int G) {
+    return ((size_t)G + (size_t)sh.nqs * c->n_seq) * 4 * c->n_kv_heads * sh.QPS;
 }
 
 struct WsLayout {
@@ -142,7 +142,7 @@ WsLayout ws_layout(const kvq_config* c, const Geometry& g) {
     for (int hpk = 1; hpk <= max_hpk; ++hpk)
         for (int T = 1; T <= c->max_t; ++T) {
             const StreamShape sh = stream_shape(c, g, hpk, T);
-            if (sh.ok) recs = std::max(recs, stream_records(c, sh, kStreamMaxGrid, hpk * c->n_kv_heads, T));
+            if (sh.ok) recs = std::max(recs, stream_records(c, sh, kStreamMaxGrid));
         }
     w.part_o = 0;
     w.part_ml = round_up(w.part_o + recs * c->head_dim * sizeof(float), 256);
@@ -333,6 +333,7 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, kvq_dtype dtyp
     p.len_d = c->len_d;
     p.base_d = c->base_d;
     p.err_d = c->err_d;
+    p.done_d = c->err_d + 1;
     p.T = T;
     p.kb = c->kb;
     p.k_tok = c->k_tok;
@@ -349,8 +350,6 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, kvq_dtype dtyp
         p.entry_offset = (long long)first;
         e = launch_append(p, sid, s);
         if (e != cudaSuccess) return cuda_fail(e, "append kernel");
-        e = launch_commit(c->len_d, sid, T, s);
-        if (e != cudaSuccess) return cuda_fail(e, "commit kernel");
     }
     for (int b : ids) {
         c->len[b] += T;
@@ -428,7 +427,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         p.NS = 3;
         while (p.NS > 2 && stream_layout(p).total > (size_t)smem_max) --p.NS;
         if (stream_layout(p).total <= (size_t)smem_max) {
-            const size_t recs = stream_records(&c->cfg, sh, p.G, n_q_heads, T);
+            const size_t recs = stream_records(&c->cfg, sh, p.G);
             if (scratch) {
                 const size_t o_ml = round_up(recs * D * sizeof(float), 256);
                 const size_t o_plan = round_up(o_ml + recs * 2 * sizeof(float), 256);

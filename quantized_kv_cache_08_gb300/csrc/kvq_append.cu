@@ -5,9 +5,10 @@
 // description): a token row keeps the [token, kv_head, dim] element order, so
 // element e = kv_head*head_dim + d of the row lands in 32-element block e/32
 // at lane e%32; K blocks are q8_0 (34 B), V blocks q5_1 (24 B).  The append
-// writes at the device slot len_d (the length before this append) and the
-// commit kernel then adds T (fields len_d / base_d, the append_kv_quantized_dc
-// and inc_seqlen steps); the physical row is slot + t - base_d.
+// writes at the device slot len_d (the length before this append) and then
+// adds T, in the same launch (fields len_d / base_d, the
+// append_kv_quantized_dc and inc_seqlen steps); the physical row is
+// slot + t - base_d.
 //
 // Rounding.  The fp16 scale of a block is the fp64 quotient rounded to fp16
 // with round-to-nearest-even (one fp64 division per block).  A code is
@@ -88,17 +89,14 @@ __device__ __forceinline__ int q5_code(float x, float m, float d, float inv) {
 }
 
 // One warp per (entry, row t, block j); lane = element of the block.
-__global__ void __launch_bounds__(256) append_kernel(AppendParams p, SeqIds ids, long long n_work) {
-    const int lane = threadIdx.x & 31;
-    const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (w >= n_work) return;
+__device__ __forceinline__ void append_block(const AppendParams& p, const SeqIds& ids, long long w, int lane) {
     const int j = (int)(w % p.kb);
     const long long rest = w / p.kb;
     const int t = (int)(rest % p.T);
     const int i = (int)(rest / p.T);
     const int b = ids.identity ? ids.first + i : ids.id[i];
-    const int slot = __ldg(p.len_d + b);
-    const int base = __ldg(p.base_d + b);
+    const int slot = p.len_d[b];                 // this launch's own commit changes len_d later
+    const int base = p.base_d[b];
     const int phys = slot + t - base;
     if (phys < 0 || phys >= p.max_rows) {
         if (lane == 0) atomicExch(p.err_d, kErrCounter);
@@ -154,10 +152,30 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p, SeqIds ids,
     }
 }
 
-__global__ void commit_kernel(int* len_d, SeqIds ids, int T) {
-    for (int i = threadIdx.x; i < ids.n; i += blockDim.x) {
-        const int b = ids.identity ? ids.first + i : ids.id[i];
-        len_d[b] += T;
+// The append of one launch, then its commit (len_d += T for the launch's
+// sequences, the inc_seqlen step): every CTA counts itself done on the
+// completion counter once its warps have read len_d, and the last one, which
+// resets the counter for the next launch, commits.
+__global__ void __launch_bounds__(256) append_kernel(AppendParams p, SeqIds ids, long long n_work) {
+    const int lane = threadIdx.x & 31;
+    const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (w < n_work) append_block(p, ids, w, lane);
+    __syncthreads();
+    __shared__ int s_last;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(p.done_d, 1) == (int)gridDim.x - 1;
+        if (s_last) {
+            *p.done_d = 0;
+            __threadfence();
+        }
+    }
+    __syncthreads();
+    if (s_last) {
+        for (int i = threadIdx.x; i < ids.n; i += blockDim.x) {
+            const int b = ids.identity ? ids.first + i : ids.id[i];
+            p.len_d[b] += p.T;
+        }
     }
 }
 
@@ -220,11 +238,6 @@ cudaError_t launch_append(const AppendParams& p, const SeqIds& ids, cudaStream_t
     if (n_work == 0) return cudaSuccess;
     const long long grid = (n_work + 7) / 8;
     append_kernel<<<(unsigned)grid, 256, 0, s>>>(p, ids, n_work);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_commit(int* len_d, const SeqIds& ids, int T, cudaStream_t s) {
-    commit_kernel<<<1, 256, 0, s>>>(len_d, ids, T);
     return cudaGetLastError();
 }
 

@@ -866,15 +866,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StreamParams 
                 ++nfrag;
             }
             if (write) {
+                // slot's records: the slice's queries, unit u's at 4 u .. 4 u + 3
                 const long long slot = (long long)blockIdx.x + (long long)qs * B + b;
-                float* po = p.part_o + slot * p.Qtot * D + dcol;
-                float* pml = p.part_ml + slot * p.Qtot * 2;
+                const int QS = 4 * p.Hkv * p.QPS;
+                float* po = p.part_o + slot * QS * D + dcol;
+                float* pml = p.part_ml + slot * QS * 2;
 #pragma unroll
                 for (int n = 0; n < 4; ++n) {
-                    const int qi = 4 * qg + n;
-                    if (qi >= p.Qh) continue;
-                    const int t = qi / p.hpk;
-                    const int off = t * p.Hq + g * p.hpk + (qi - t * p.hpk);   // t * Hq + h
+                    if (4 * qg + n >= p.Qh) continue;
+                    const int off = 4 * u + n;
                     if (lane < VH) {
                         float* dst = po + (size_t)off * D;
                         *reinterpret_cast<float4*>(dst) = make_float4(o2[n][0].x, o2[n][0].y, o2[n][1].x, o2[n][1].y);
@@ -948,6 +948,9 @@ __global__ void __launch_bounds__(kThreads) merge_stream_kernel(const MergeStrea
     const int t = qg / p.Hq, h = qg - t * p.Hq;
     const int qi = t * p.hpk + (h % p.hpk);
     const int qs = (qi >> 2) / p.QPS;
+    // the query's record in a slot: unit (KV head, query group in the slice), member
+    const int QS = 4 * (p.Hq / p.hpk) * p.QPS;
+    const int qloc = ((h / p.hpk) * p.QPS + (qi >> 2) - qs * p.QPS) * 4 + (qi & 3);
     const int key = qs * p.B + b;
     const int xa = qs * R + p.plan[b];
     const int xb = xa + (p.plan[b + 1] - p.plan[b]);
@@ -974,7 +977,7 @@ __global__ void __launch_bounds__(kThreads) merge_stream_kernel(const MergeStrea
             if (ok) {
                 const int c = c_lo + r;
                 ok = starts[c + 1] > starts[c];               // an empty CTA range wrote nothing
-                rec = (long long)(c + key) * p.Qtot + qg;
+                rec = (long long)(c + key) * QS + qloc;
             }
             const float2 mlv = ok ? *reinterpret_cast<const float2*>(p.part_ml + rec * 2) : make_float2(kNegInf, 0.f);
             m4[u] = mlv.x;

@@ -38,9 +38,10 @@ struct AppendParams {
     int bf16;
     uint8_t* k_plane;              // [B][max_rows][k_tok]
     uint8_t* v_plane;              // [B][max_rows][v_tok]
-    const int* len_d;
+    int* len_d;                    // read for the slot, then advanced by T (the launch's last CTA)
     const int* base_d;
     int* err_d;
+    int* done_d;                   // completion counter of the launch's CTAs (0 between launches)
     int T, kb, k_tok, v_tok, max_rows;
     int fp8;                       // 1: both planes hold FP8 E4M3 bytes
     long long entry_offset;        // first input entry of this launch
@@ -130,8 +131,8 @@ struct StreamParams {
     int NS;                        // stages of each of the K and V rings
     uint32_t Sk, Sv;               // shared-memory row strides of the K and V stages
     int qbits;                     // 16 or 24: query quantisation
-    float* part_o;                 // [slot][Qtot][D]
-    float* part_ml;                // [slot][Qtot][2]  (max in log2 units, sum)
+    float* part_o;                 // [slot][4 Hkv QPS][D]: the slice's queries, unit-major
+    float* part_ml;                // [slot][4 Hkv QPS][2]  (max in log2 units, sum)
     int* plan;                     // [B+1] prefix of visible rows, then [G+1] CTA range starts
 };
 
@@ -200,8 +201,8 @@ struct MergeParams {
 };
 
 // launchers (kvq_append.cu)
+// quantised append of a launch's sequences, then len_d += T for them
 cudaError_t launch_append(const AppendParams& p, const SeqIds& ids, cudaStream_t s);
-cudaError_t launch_commit(int* len_d, const SeqIds& ids, int T, cudaStream_t s);
 cudaError_t launch_set_len(int* len_d, const SeqIds& ids, const int* values, cudaStream_t s);
 cudaError_t launch_ring_copy(const uint8_t* src_k, const uint8_t* src_v, uint8_t* dst_k,
                              uint8_t* dst_v, size_t k_bytes, size_t v_bytes, cudaStream_t s);

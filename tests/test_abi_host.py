@@ -75,7 +75,7 @@ def test_bytes_per_token_and_required_sizes(L):
     (dict(head_dim=0), B.KVQ_EINVAL),
     (dict(max_q_heads=12, n_kv_heads=8), B.KVQ_EINVAL),
     (dict(max_t=0), B.KVQ_EINVAL),
-    (dict(max_t=65), B.KVQ_EINVAL),
+    (dict(max_t=513), B.KVQ_EINVAL),
     (dict(ring=1, window=0), B.KVQ_EINVAL),
     (dict(ring=1, window=100, max_rows=100), B.KVQ_EINVAL),
     (dict(n_seq=0), B.KVQ_EINVAL),

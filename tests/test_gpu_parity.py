@@ -327,6 +327,36 @@ def test_ring_multi_row_chunks_match_windowed_oracle(path):
     assert p.dev.device_error() == 0
 
 
+@pytest.mark.parametrize("path", [1, 2])
+def test_ring_prime_chunks_match_windowed_oracle(path):
+    """Prefill-sized chunks on the ring ("Module cache": the ring carries one
+    whole maximum-size prime chunk beside the window): max_t = 512, the ring
+    sized window + 30 + 512, chunks of up to 512 rows mixed with short ones,
+    each followed by its causal T-row decode; outputs match the windowed
+    oracle and the live rows its bytes, across rebases."""
+    Hq, Hkv, D, W, MT = 16, 4, 64, 1024, 512
+    chunks = [512, 512, 100, 1, 512, 300, 7, 512, 33, 512, 1, 2, 512]
+    N = sum(chunks)
+    p = Pair(1, Hkv, D, Hq, max_t=MT, window=W, ring=True)
+    p.dev.set_decode_path(path)
+    assert p.dev.rows == W + 30 + MT
+    k = _randn(1, N, Hkv, D, seed=121)
+    v = _randn(1, N, Hkv, D, seed=122)
+    s = _randn(Hq, seed=123)
+    L = 0
+    for step, T in enumerate(chunks):
+        p.append(k[:, L:L + T], v[:, L:L + T])
+        L += T
+        base = p.dev.bases()[0]
+        lstart = max(0, L - T + 1 - W)
+        assert base <= lstart and L - base <= p.dev.rows
+        got, ref = p.decode(_randn(1, T, Hq, D, seed=3000 + step), sinks=s)
+        assert_close(got, ref, what=f"chunk {step} (T={T}, len {L})")
+        assert_rows_equal(p.dev, p.ora, 0, lstart, L)
+    assert p.dev.bases()[0] > 0
+    assert p.dev.device_error() == 0
+
+
 @pytest.mark.parametrize("path", [(0, 0), (1, 0), (2, 16)], ids=["auto", "generic", "stream"])
 @pytest.mark.parametrize("shape", [
     # B, Hq, Hkv, D, lens, T, window, sinks
