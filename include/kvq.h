@@ -99,21 +99,31 @@ typedef struct kvq_config {
     kvq_fmt v_fmt;    /* v_fmt KVQ_FP8_E4M3; no other pairs                        */
 } kvq_config;
 
-/* Device bytes the caller provides (each buffer 16-byte aligned):
- *   k_plane   [n_seq][max_rows][kb*34]  kb = n_kv_heads*head_dim/32, plus
- *             128 bytes of padding (tile copies move whole 128-byte column
- *             blocks), rounded up to a multiple of 256 bytes
- *   v_plane   [n_seq][max_rows][kb*24]  (padded and rounded likewise)
- *             With FP8 E4M3 both planes are [n_seq][max_rows][kb*32].
- *   counters  len_d[n_seq], base_d[n_seq], error word, work-item counter (int32)
- *   workspace decode partials, the split plan and the ring-rebase scratch   */
+/* Device bytes the caller provides (each buffer 16-byte aligned), and the
+ * geometry they hold ("Module cache", fn cache_bytes_per_token and
+ * fn swa_ring_rows):
+ *   k_plane   [n_seq][rows][k_row_bytes], k_row_bytes = kb*34,
+ *             kb = n_kv_heads*head_dim/32, plus 128 bytes of padding (the
+ *             generic decode's tile copies may pass the last row), rounded up
+ *             to a multiple of 256 bytes
+ *   v_plane   [n_seq][rows][v_row_bytes], v_row_bytes = kb*24 (padded and
+ *             rounded likewise).  With FP8 E4M3 both rows are kb*32 bytes.
+ *   counters  len_d[n_seq], base_d[n_seq], error word, the append's
+ *             completion counter, the ring rebase's barrier words (int32)
+ *   workspace decode partials, the split plan and the ring-rebase scratch
+ *   rows      physical rows per sequence: max_rows for a flat cache, and for
+ *             a ring max_rows or, when it is 0, window + 30 + max_t        */
 typedef struct kvq_sizes {
     size_t k_plane, v_plane, counters, workspace;
+    int rows, k_row_bytes, v_row_bytes;
 } kvq_sizes;
 
 typedef struct kvq_cache kvq_cache;
 
-/* Sizes of the four device buffers for a configuration.  Pure host call. */
+/* Sizes of the four device buffers for a configuration and the rows they
+ * hold (fn new of "Struct Cache" allocates by geometry and maximum context;
+ * the byte counts per row are fn cache_bytes_per_token's for one layer).
+ * Pure host call: KVQ_EINVAL / KVQ_EUNSUPPORTED for a bad configuration. */
 kvq_status kvq_required_bytes(const kvq_config* cfg, kvq_sizes* out);
 
 /* Build a cache over caller buffers (fn new of "Struct Cache").  Validates the
@@ -127,7 +137,9 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane,
                      void* counters, void* workspace, void* stream,
                      kvq_cache** out);
 
-/* Release the host handle (device buffers stay the caller's). NULL is a no-op. */
+/* Release the host handle (device buffers stay the caller's).  NULL is a
+ * no-op.  No passage: the pages' cache owns its memory, this one only a
+ * host handle. */
 void kvq_free(kvq_cache* cache);
 
 /* Quantised append ("Struct KvLayer": append_kv_quantized_dc[w] writes at the
@@ -139,7 +151,10 @@ void kvq_free(kvq_cache* cache);
  * whose live rows would overflow the ring: logical rows [new_base, len) with
  * new_base = max(0, len + 1 - window) rounded down to a multiple of 32 move to
  * physical row 0 and base becomes new_base (fn swa_ring_rows: at most 31
- * masked rows precede the live window).  Host lengths advance by T. */
+ * masked rows precede the live window).  The move is one cooperative launch
+ * through shared memory when the rows are 16-byte multiples and the live
+ * bytes fit the SMs' shared memory, else two copies through the workspace.
+ * Host lengths advance by T. */
 kvq_status kvq_append(kvq_cache* cache, const void* k, const void* v,
                       kvq_dtype dtype, int T, const int* seq_ids, int n_ids,
                       void* stream);
@@ -153,7 +168,12 @@ kvq_status kvq_append(kvq_cache* cache, const void* k, const void* v,
  * (scale <= 0 selects 1/sqrt(D)); sinks (device [n_q_heads] f32, or NULL) are
  * unscaled logits joining the max and the denominator with no value.
  * out: device f32 [n_seq][T][n_q_heads][D].  Every sequence needs len >= T.
- * Runs a split kernel over (sequence, row chunk) work items and a merge. */
+ * Two launches: a split kernel writes partial softmax records (running max,
+ * denominator, unnormalised output) and a merge kernel combines them with the
+ * sinks.  The split kernel is the stream-K kernel (its CTAs, at most one per
+ * SM, each take an equal share of all sequences' visible rows in 32-row
+ * tiles) or the generic kernel over (sequence, row chunk) work items; see
+ * kvq_set_decode_path. */
 kvq_status kvq_decode(kvq_cache* cache, const void* q, kvq_dtype dtype, int T,
                       int n_q_heads, const float* sinks, float scale,
                       float* out, void* stream);
@@ -167,13 +187,21 @@ kvq_status kvq_decode(kvq_cache* cache, const void* q, kvq_dtype dtype, int T,
  * kvq_decode (the same kernels run on the same split plan), but the split
  * partials and the plan live in a file-scope device array of
  * KVQ_NOALLOC_SCRATCH_BYTES (16 MiB) inside the library: the call allocates
- * nothing.  The decode needs n_seq * ceil(max visible rows / split rows) *
- * n_q_heads * T * (head_dim + 2) * 4 bytes plus the plan; a call that needs
- * more returns KVQ_ERANGE (nothing launched) and says how much.  Nothing in
- * the array has to start at zero: every byte read was written earlier in the
- * same call.  The first call on a device resolves the array's address
- * (cudaGetSymbolAddress, with that device current): make it before any stream
- * capture.  All calls share the one array per device, so two calls whose
+ * nothing.  The decode needs R records of (head_dim + 2) * 4 bytes plus its
+ * plan.  On the stream-K kernel R = (G + nqs * n_seq) * 4 * Hkv * QPS and the
+ * plan is n_seq + 2 + G ints, where G <= 256 is the CTA count (one per SM at
+ * most), u = ceil(hpk * T / 4) four-query units per KV head (hpk =
+ * n_q_heads / Hkv), QPS = max(1, min(u, 16 / Hkv)) and nqs = ceil(u / QPS):
+ * 64 sequences with 8 KV heads, 32 Q heads and T = 1 need about 3.6 MB on 152
+ * SMs.  On the generic kernel R = n_seq * ceil(max visible rows / split rows)
+ * * n_q_heads * T and the plan is n_seq + 1 ints.  A call that needs more
+ * returns KVQ_ERANGE (nothing launched) and says how much.  Nothing in the
+ * array has to start at zero: every byte read was written earlier in the
+ * same call.  The array's address is resolved (cudaGetSymbolAddress, with the
+ * device current) on the first call on a device and again whenever the
+ * calling thread's current CUDA context differs from the one it was resolved
+ * in: make the first call in each context before any stream capture.  All
+ * calls share the one array per device, so two calls whose
  * kernels may overlap (other streams, other threads, other caches) race:
  * order them on one stream or synchronise between them. */
 kvq_status kvq_decode_noalloc(kvq_cache* cache, const void* q, kvq_dtype dtype, int T,
@@ -214,8 +242,9 @@ kvq_status kvq_truncate_device(kvq_cache* cache, const int* accept_d, int T, voi
 kvq_status kvq_sync_len(kvq_cache* cache, void* stream);
 
 /* Host mirror of the lengths and ring bases (HOST arrays of n_seq ints;
- * either pointer may be NULL).  After kvq_truncate_device and before
- * kvq_sync_len the lengths are upper bounds. */
+ * either pointer may be NULL): the host side of the len_d / base_d pair of
+ * "Struct KvLayer".  After kvq_truncate_device and before kvq_sync_len the
+ * lengths are upper bounds. */
 kvq_status kvq_get_len(const kvq_cache* cache, int* len_host, int* base_host);
 
 /* Advance the host mirror after `steps` replays of a captured graph that
@@ -238,20 +267,19 @@ kvq_status kvq_physical_rows(const kvq_cache* cache, int seq, int start,
  * out) and clear it. */
 kvq_status kvq_read_device_error(kvq_cache* cache, int* err, void* stream);
 
-/* Choose the decode kernel: path 0 = automatic (the warp-specialised kernel
- * whenever the formats are q8_0/q5_1, token rows are 16-byte multiples,
- * n_kv_heads <= 8,
- * (queries per KV head rounded up to 4 or 8) / 4 * n_kv_heads * head_dim / 32
- * is a power of two <= 128, and its tiles fit shared memory, else the generic
- * split kernel), 1 = generic, 2 = warp-specialised
- * (KVQ_EUNSUPPORTED at decode time if the geometry or format does not allow
- * it; FP8 E4M3 caches always decode on the generic kernel).
- * query_bits (0 = 16, or 16, or 24): the warp-specialised kernel quantises
+/* Choose the decode kernel: path 0 = automatic (the stream-K kernel whenever
+ * it allows the cache and the call, else the generic split kernel),
+ * 1 = generic, 2 = stream-K (KVQ_EUNSUPPORTED at decode time if it does not
+ * allow them).  The stream-K kernel needs the q8_0/q5_1 formats, K and V
+ * token rows that are 16-byte multiples (n_kv_heads * head_dim a multiple of
+ * 256), head_dim 64, 128 or 256, n_kv_heads <= 16, n_seq <= 1024 and its
+ * tiles within shared memory; FP8 E4M3 caches always decode on the generic
+ * kernel.  query_bits (0 = 16, or 16, or 24): the stream-K kernel quantises
  * each pre-scaled query element per 32-element block to this many bits
- * against the block's largest magnitude and multiplies with int8 dot
- * products; 16 bits adds an error below 1e-4 to the attention output on
- * unit-variance data, 24 bits is at the level of fp32 rounding and costs a
- * third more dot products. */
+ * against the block's largest magnitude and multiplies it with the int8 K
+ * codes in integer dot products; 16 bits adds an error below 1e-4 to the
+ * attention output on unit-variance data, 24 bits is at the level of fp32
+ * rounding and costs half again as many dot products. */
 kvq_status kvq_set_decode_path(kvq_cache* cache, int path, int query_bits);
 
 /* Score soft-capping for later decodes ("Struct LayerKvCache": the softcap
@@ -259,12 +287,13 @@ kvq_status kvq_set_decode_path(kvq_cache* cache, int path, int query_bits);
  * without defining; read as the usual logit soft-capping).  softcap > 0 maps
  * every scaled score s = scale * <q, k_hat> to softcap * tanh(s / softcap)
  * before the softmax; sink logits are not capped.  0 (the default) turns it
- * off.  While a cap is set, decodes run the generic split kernel (a decode
- * forced onto the warp-specialised kernel with kvq_set_decode_path path 2
- * returns KVQ_EUNSUPPORTED).  KVQ_EINVAL for a negative or non-finite value. */
+ * off.  Both decode kernels apply it.  KVQ_EINVAL for a negative or
+ * non-finite value. */
 kvq_status kvq_set_softcap(kvq_cache* cache, float softcap);
 
-/* Override the decode split size in rows (a multiple of 8, >= 64; 0 = auto). */
+/* Override the generic kernel's split size in rows (a multiple of 8, >= 64;
+ * 0 = auto).  The stream-K kernel ignores it: its CTAs split the rows
+ * evenly. */
 kvq_status kvq_set_split_rows(kvq_cache* cache, int rows);
 
 /* Bytes per 32-element block of a format: 34 (q8_0), 24 (q5_1) or 32
@@ -276,7 +305,8 @@ int kvq_block_bytes(kvq_fmt fmt);
  * input. */
 size_t kvq_bytes_per_token(const kvq_config* cfg);
 
-/* Message of the last failed call on this thread ("" if none). */
+/* Message of the last failed call on this thread ("" if none).  No passage:
+ * error reporting of this C interface. */
 const char* kvq_last_error(void);
 
 #ifdef __cplusplus

@@ -49,7 +49,8 @@ class kvq_config(ctypes.Structure):
 
 class kvq_sizes(ctypes.Structure):
     _fields_ = [("k_plane", ctypes.c_size_t), ("v_plane", ctypes.c_size_t),
-                ("counters", ctypes.c_size_t), ("workspace", ctypes.c_size_t)]
+                ("counters", ctypes.c_size_t), ("workspace", ctypes.c_size_t),
+                ("rows", ctypes.c_int), ("k_row_bytes", ctypes.c_int), ("v_row_bytes", ctypes.c_int)]
 
 
 _LIB = None

@@ -43,7 +43,7 @@ class KVCache:
                  window=0, ring=False, device=None, stream=None, fmt="q8_0/q5_1"):
         if fmt not in self.FORMATS:
             raise ValueError(f"fmt must be one of {sorted(self.FORMATS)}")
-        k_fmt, v_fmt, k_blk, v_blk = self.FORMATS[fmt]
+        k_fmt, v_fmt, _, _ = self.FORMATS[fmt]
         self.fmt = fmt
         self.cfg = B.make_config(n_seq, n_kv_heads, head_dim, max_q_heads, max_t, max_rows,
                                  window, ring, k_fmt, v_fmt)
@@ -54,12 +54,8 @@ class KVCache:
         self.counters = torch.empty(sz.counters // 4, dtype=torch.int32, device=dev)
         self.workspace = torch.empty(max(sz.workspace, 16), dtype=torch.uint8, device=dev)
         self.n_seq, self.n_kv_heads, self.head_dim = n_seq, n_kv_heads, head_dim
-        kb = n_kv_heads * head_dim // 32
-        self.k_tok, self.v_tok = kb * k_blk, kb * v_blk
-        if ring:
-            self.rows = max_rows if max_rows else window + 30 + max_t
-        else:
-            self.rows = max_rows
+        # the geometry as the library lays it out
+        self.k_tok, self.v_tok, self.rows = sz.k_row_bytes, sz.v_row_bytes, sz.rows
         self.window, self.ring = window, bool(ring)
         self.handle = B.kvq_alloc(self.cfg, self.k_plane.data_ptr(), self.v_plane.data_ptr(),
                                   self.counters.data_ptr(), self.workspace.data_ptr(),

@@ -113,10 +113,10 @@ StreamShape stream_shape(const kvq_config* c, const Geometry& g, int hpk, int T)
     StreamShape sh{false, 1, 1, 1};
     const int NBH = c->head_dim / 32;
     if (g.fp8 || g.k_tok % 16 || g.v_tok % 16 || !(NBH == 2 || NBH == 4 || NBH == 8) || c->n_seq > kStreamMaxB ||
-        c->n_kv_heads > 16)
+        c->n_kv_heads > kStreamThreads / 32)
         return sh;
     const int nQG = (hpk * T + 3) / 4;
-    sh.QPS = std::max(1, std::min(nQG, 16 / c->n_kv_heads));
+    sh.QPS = std::max(1, std::min(nQG, (kStreamThreads / 32) / c->n_kv_heads));
     sh.nqs = (nQG + sh.QPS - 1) / sh.QPS;
     const int nU = c->n_kv_heads * sh.QPS;
     sh.RS = 2 * nU <= kStreamThreads / 32 ? 2 : 1;
@@ -152,7 +152,9 @@ WsLayout ws_layout(const kvq_config* c, const Geometry& g) {
     return w;
 }
 
-size_t counters_bytes(int n_seq) { return round_up((2 * (size_t)n_seq + 2) * sizeof(int), 256); }
+// len_d[n], base_d[n], error word, append completion counter, rebase arrival
+// counter, rebase barrier generation
+size_t counters_bytes(int n_seq) { return round_up((2 * (size_t)n_seq + 4) * sizeof(int), 256); }
 
 // visible-row start of a T-row step
 int vis_lo(const kvq_cache* c, int len, int T) {
@@ -191,6 +193,9 @@ kvq_status kvq_required_bytes(const kvq_config* cfg, kvq_sizes* out) {
     out->v_plane = round_up((size_t)cfg->n_seq * g.rows * g.v_tok + 128, 256);
     out->counters = counters_bytes(cfg->n_seq);
     out->workspace = ws_layout(cfg, g).total;
+    out->rows = g.rows;
+    out->k_row_bytes = g.k_tok;
+    out->v_row_bytes = g.v_tok;
     return KVQ_OK;
 }
 
@@ -314,6 +319,15 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, kvq_dtype dtyp
         uint8_t* sk = c->ws + c->off_scratch;
         uint8_t* sv = sk + (size_t)c->rows * c->k_tok;
         const size_t kbytes = (size_t)live * c->k_tok, vbytes = (size_t)live * c->v_tok;
+        // one pass through shared memory when it fits, else two copy legs
+        // through the workspace scratch
+        if (launch_rebase_one_pass(c->k_plane + src_row * c->k_tok, c->v_plane + src_row * c->v_tok,
+                                   c->k_plane + dst_row * c->k_tok, c->v_plane + dst_row * c->v_tok, kbytes, vbytes,
+                                   c->base_d, b, nb, c->err_d + 2, c->err_d + 3, c->err_d, c->num_sms, s, &e)) {
+            if (e != cudaSuccess) return cuda_fail(e, "ring rebase");
+            c->base[b] = nb;
+            continue;
+        }
         e = launch_ring_copy(c->k_plane + src_row * c->k_tok, c->v_plane + src_row * c->v_tok, sk, sv, kbytes,
                              vbytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "ring rebase copy");
@@ -422,7 +436,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         // CTAs: one per SM, fewer when there are fewer 32-row tiles of work
         const long long work = total_vis * sh.nqs;
         p.G = (int)std::max(1LL, std::min<long long>((work + kStreamRows - 1) / kStreamRows,
-                                                     std::min(c->num_sms, kStreamMaxGrid)));
+                                                     std::min(kStreamCtasPerSm * c->num_sms, kStreamMaxGrid)));
         const int smem_max = stream_max_smem();
         p.NS = 3;
         while (p.NS > 2 && stream_layout(p).total > (size_t)smem_max) --p.NS;
@@ -580,26 +594,52 @@ kvq_status kvq_decode(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n
 }
 
 // Decode scratch of kvq_decode_noalloc: one file-scope device array per
-// device (the module's copy on each device), resolved once per device.
+// device (the module's copy on each device).  Its address is resolved with
+// that device current the first time, and again whenever the device's current
+// context is a different one (after cudaDeviceReset the module is loaded anew
+// and the array may move).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+static void* current_context() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    static GetCurrent get = nullptr;
+    if (!get) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return nullptr;
+        get = reinterpret_cast<GetCurrent>(fn);
+    }
+    CUcontext ctx = nullptr;
+    return get(&ctx) == CUDA_SUCCESS ? static_cast<void*>(ctx) : nullptr;
+}
 
 kvq_status kvq_decode_noalloc(kvq_cache* c, const void* q, kvq_dtype dtype, int T, int n_q_heads,
                               const float* sinks, float scale, float* out, void* stream) {
     static std::mutex mu;
     static void* addr[kMaxDevices] = {};
+    static void* ctx_of[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(KVQ_EUNSUPPORTED, "device %d beyond %d devices", dev, kMaxDevices);
+    void* ctx = current_context();
+    void* a = nullptr;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (!addr[dev]) {
+        if (!addr[dev] || ctx_of[dev] != ctx) {
             e = cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the no-alloc scratch");
+            if (e != cudaSuccess) {
+                addr[dev] = nullptr;
+                return cuda_fail(e, "cudaGetSymbolAddress of the no-alloc scratch");
+            }
+            ctx_of[dev] = ctx;
         }
+        a = addr[dev];
     }
-    return decode_impl(c, q, dtype, T, n_q_heads, sinks, scale, out, stream,
-                       static_cast<unsigned char*>(addr[dev]), KVQ_NOALLOC_SCRATCH_BYTES);
+    return decode_impl(c, q, dtype, T, n_q_heads, sinks, scale, out, stream, static_cast<unsigned char*>(a),
+                       KVQ_NOALLOC_SCRATCH_BYTES);
 }
 
 kvq_status kvq_truncate(kvq_cache* c, const int* new_len, void* stream) {

@@ -28,6 +28,8 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
 namespace kvq {
 namespace {
 
@@ -231,6 +233,56 @@ __global__ void __launch_bounds__(256) ring_copy_kernel(const uint4* __restrict_
     }
 }
 
+// Ring rebase in one pass: logical rows [new_base, len) of a sequence move
+// to physical row 0 ("Struct KvLayer", field base_d: physical = row - base;
+// "Module cache", fn swa_ring_rows).  The destination overlaps the source, so
+// every CTA first reads its share of the live bytes of both planes into shared
+// memory, all CTAs meet at a grid barrier (the launch is cooperative, so they
+// are all resident), then write; CTA 0 then sets base_d.  A barrier that does
+// not complete within ~1 s sets the error word and nothing is written.
+__global__ void __launch_bounds__(256) rebase_kernel(const uint4* sk, uint4* dk, size_t nk16, const uint4* sv,
+                                                     uint4* dv, size_t nv16, int* base_d, int seq, int new_base,
+                                                     int* arrive, int* gen, int* err_d) {
+    extern __shared__ uint4 buf[];
+    const size_t total = nk16 + nv16;
+    const size_t per = (total + gridDim.x - 1) / gridDim.x;
+    const size_t lo = (size_t)blockIdx.x * per;
+    const size_t hi = lo + per < total ? lo + per : total;
+    for (size_t i = lo + threadIdx.x; i < hi; i += blockDim.x) buf[i - lo] = i < nk16 ? sk[i] : sv[i - nk16];
+    __syncthreads();
+    __shared__ int s_ok;
+    if (threadIdx.x == 0) {
+        // sense-reversing grid barrier: the last arrival opens the next generation
+        const int g0 = *(volatile int*)gen;
+        __threadfence();
+        if (atomicAdd(arrive, 1) == (int)gridDim.x - 1) {
+            *arrive = 0;
+            __threadfence();
+            atomicAdd(gen, 1);
+            s_ok = 1;
+        } else {
+            const long long t0 = clock64();
+            s_ok = 1;
+            while (*(volatile int*)gen == g0) {
+                if (clock64() - t0 > (1LL << 31)) {
+                    atomicExch(err_d, kErrWait);
+                    s_ok = 0;
+                    break;
+                }
+                __nanosleep(200);
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    if (!s_ok) return;
+    for (size_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        if (i < nk16) dk[i] = buf[i - lo];
+        else dv[i - nk16] = buf[i - lo];
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) base_d[seq] = new_base;
+}
+
 }  // namespace
 
 cudaError_t launch_append(const AppendParams& p, const SeqIds& ids, cudaStream_t s) {
@@ -278,6 +330,48 @@ cudaError_t launch_truncate_accept(int* len_d, const int* base_d, int* err_d, co
                                    int window, int ring, cudaStream_t s) {
     truncate_accept_kernel<<<(n + 255) / 256, 256, 0, s>>>(len_d, base_d, err_d, accept_d, n, T, window, ring);
     return cudaGetLastError();
+}
+
+bool launch_rebase_one_pass(const uint8_t* src_k, const uint8_t* src_v, uint8_t* dst_k, uint8_t* dst_v,
+                            size_t k_bytes, size_t v_bytes, int* base_d, int seq, int new_base, int* arrive,
+                            int* gen, int* err_d, int num_sms, cudaStream_t s, cudaError_t* err) {
+    *err = cudaSuccess;
+    if (((k_bytes | v_bytes | (size_t)src_k | (size_t)src_v | (size_t)dst_k | (size_t)dst_v) & 15) != 0)
+        return false;
+    const size_t total = (k_bytes + v_bytes) / 16;
+    if (total == 0) return false;
+    const int grid = (int)std::min<size_t>((size_t)num_sms, (total + 255) / 256);
+    const size_t per = (total + grid - 1) / grid;
+    const size_t smem = per * 16;
+    static std::atomic<unsigned long long> attrs{0};
+    cudaError_t e = kernel_attrs_once(rebase_kernel, attrs, true);
+    if (e != cudaSuccess) {
+        *err = e;
+        return true;
+    }
+    int dev = 0, optin = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (smem + 1024 > (size_t)optin) return false;      // too large for one pass
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, rebase_kernel, reinterpret_cast<const uint4*>(src_k), reinterpret_cast<uint4*>(dst_k),
+                           k_bytes / 16, reinterpret_cast<const uint4*>(src_v), reinterpret_cast<uint4*>(dst_v),
+                           v_bytes / 16, base_d, seq, new_base, arrive, gen, err_d);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    *err = e != cudaSuccess ? e : cudaGetLastError();
+    return true;
 }
 
 cudaError_t launch_set_base(int* base_d, int seq, int value, cudaStream_t s) {

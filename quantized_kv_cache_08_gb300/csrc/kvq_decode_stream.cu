@@ -52,6 +52,8 @@ using namespace dev;
 
 constexpr int kThreads = kStreamThreads;
 constexpr int kWarps = kThreads / 32;
+constexpr int kMergeThreads = 512;
+constexpr int kMergeWarps = kMergeThreads / 32;
 constexpr int kRows = kStreamRows;
 constexpr long long kWaitCycles = 1LL << 31;   // ~1 s bound on any mbarrier wait
 
@@ -458,11 +460,13 @@ __device__ __forceinline__ void v_row(const uint8_t* vb, int h, uint32_t sel_lo,
 // ------------------------------------------------------------ the kernel
 
 template <int NBH, int KP, int NQB>
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StreamParams p,
+__global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(const StreamParams p,
                                                               const __grid_constant__ CUtensorMap kmap,
                                                               const __grid_constant__ CUtensorMap vmap) {
     constexpr int D = NBH * 32;
-    constexpr int RW = kRows / KP;      // rows of a tile per warp (KP = RS)
+    constexpr int RW = 32 / KP;         // rows of a tile per warp: RW rows x KP lanes
+    constexpr int RS = kRows / RW;      // row slices of a tile: warps per unit
+    static_assert(RS >= 1 && RS <= 2 && RS * RW == kRows, "a tile splits into one or two row slices");
     constexpr int QPL = 4 / KP;         // queries per lane in the K phase
     constexpr int VH = 2 * NBH;         // half blocks per head: V lanes per row group
     constexpr int RG = 32 / VH;         // V row groups
@@ -584,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StreamParams 
     if (warp >= p.NA) return;
 
     // ---- this warp: unit (KV head g, query group qgl of a slice), row slice rs
-    const int u = warp / KP, rs = warp - u * KP;
+    const int u = warp / RS, rs = warp - u * RS;
     const int g = u / p.QPS, qgl = u - g * p.QPS;
     const uint32_t w_off = (uint32_t)L.W + (uint32_t)warp * L.wwarp;
     const uint32_t lw_off = (uint32_t)L.LW + (uint32_t)warp * L.lwarp;
@@ -809,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StreamParams 
             }
             const int dcol = vi * 32 + 8 * vh;          // the lane's dims: dcol + 0..7, dcol + 16..23
             bool write = true;
-            if constexpr (KP == 2) {
+            if constexpr (RS == 2) {
                 float* so = reinterpret_cast<float*>(smem + L.CB + (size_t)u * (16 * D + 32));   // [4][D], m[4], l[4]
                 float* sml = so + 4 * D;
                 const uint32_t pf = smem_u32(&s_pair[2 * u]), pe = smem_u32(&s_pair[2 * u + 1]);
@@ -925,10 +929,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StreamParams 
 // folding every WPQ-th record with U records' loads in flight, and their
 // states meet in shared memory.
 template <int VPL, int U>
-__global__ void __launch_bounds__(kThreads) merge_stream_kernel(const MergeStreamParams p) {
+__global__ void __launch_bounds__(kMergeThreads) merge_stream_kernel(const MergeStreamParams p) {
     extern __shared__ float msm[];                   // [pairs][WPQ][2 + DC]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int PPC = kWarps / p.WPQ;
+    const int PPC = kMergeWarps / p.WPQ;
     const int pl = warp / p.WPQ, sub = warp - pl * p.WPQ;
     const int DC = 32 * VPL;
     const int NCH = p.D / DC;
@@ -1061,16 +1065,16 @@ cudaError_t launch_stream_t(const StreamParams& p, const CUtensorMap& kmap, cons
 
 template <int VPL, int U>
 cudaError_t launch_merge_stream_t(const MergeStreamParams& p, cudaStream_t s) {
-    const int PPC = kWarps / p.WPQ;
+    const int PPC = kMergeWarps / p.WPQ;
     const long long npairs = (long long)p.B * p.Qtot * (p.D / (32 * VPL));
-    const size_t smem = (size_t)kWarps * (2 + 32 * VPL) * sizeof(float);
+    const size_t smem = (size_t)kMergeWarps * (2 + 32 * VPL) * sizeof(float);
     auto fn = merge_stream_kernel<VPL, U>;
     static std::atomic<unsigned long long> attrs{0};
     cudaError_t e = kernel_attrs_once(fn, attrs, true);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((npairs + PPC - 1) / PPC), 1, 1);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1089,8 +1093,9 @@ cudaError_t launch_split_stream(const StreamParams& p, const CUtensorMap& kmap, 
                                 cudaStream_t s) {
     const size_t smem = stream_layout(p).total;
     const int NBH = p.D / 32;
+    const int KP = p.RS * 32 / kStreamRows;       // lanes per row in the key phase
 #define KVQ_CASE(nb, kp, nq) \
-    if (NBH == nb && p.RS == kp && p.qbits == nq) return launch_stream_t<nb, kp, nq>(p, kmap, vmap, smem, s);
+    if (NBH == nb && KP == kp && p.qbits == nq) return launch_stream_t<nb, kp, nq>(p, kmap, vmap, smem, s);
     KVQ_CASE(2, 1, 16) KVQ_CASE(2, 2, 16) KVQ_CASE(4, 1, 16) KVQ_CASE(4, 2, 16) KVQ_CASE(8, 1, 16) KVQ_CASE(8, 2, 16)
     KVQ_CASE(2, 1, 24) KVQ_CASE(2, 2, 24) KVQ_CASE(4, 1, 24) KVQ_CASE(4, 2, 24) KVQ_CASE(8, 1, 24) KVQ_CASE(8, 2, 24)
 #undef KVQ_CASE

@@ -107,6 +107,7 @@ inline cudaError_t kernel_attrs_once(F fn, std::atomic<unsigned long long>& done
 // partials to record slot c + key, key = slice * B + sequence.
 constexpr int kStreamThreads = 512;     // 16 warps, one (KV head, 4 queries) unit and row slice each
 constexpr int kStreamRows = 32;         // token rows per tile
+constexpr int kStreamCtasPerSm = 1;
 constexpr int kStreamMaxB = 1024;       // sequences the per-CTA tables hold
 constexpr int kStreamMaxGrid = 256;     // most CTAs a decode may use (record slots are sized by it)
 
@@ -207,6 +208,13 @@ cudaError_t launch_set_len(int* len_d, const SeqIds& ids, const int* values, cud
 cudaError_t launch_ring_copy(const uint8_t* src_k, const uint8_t* src_v, uint8_t* dst_k,
                              uint8_t* dst_v, size_t k_bytes, size_t v_bytes, cudaStream_t s);
 cudaError_t launch_set_base(int* base_d, int seq, int value, cudaStream_t s);
+// one-pass ring rebase (move the live rows to physical row 0, then base_d =
+// new_base) when the rows are 16-byte aligned and the live bytes fit the SMs'
+// shared memory: returns false (nothing launched) otherwise; *err reports a
+// failed launch
+bool launch_rebase_one_pass(const uint8_t* src_k, const uint8_t* src_v, uint8_t* dst_k, uint8_t* dst_v,
+                            size_t k_bytes, size_t v_bytes, int* base_d, int seq, int new_base, int* arrive,
+                            int* gen, int* err_d, int num_sms, cudaStream_t s, cudaError_t* err);
 // len_d[b] -= T - accept_d[b] for b < n, checked on the device (error word on failure)
 cudaError_t launch_truncate_accept(int* len_d, const int* base_d, int* err_d, const int* accept_d, int n, int T,
                                    int window, int ring, cudaStream_t s);

@@ -357,6 +357,40 @@ def test_ring_prime_chunks_match_windowed_oracle(path):
     assert p.dev.device_error() == 0
 
 
+@pytest.mark.parametrize("shape", [
+    # Hq, Hkv, D, W, MT, N: rows of 68 + 48 bytes (not 16-byte multiples)
+    (4, 1, 64, 300, 64, 2000),
+    # 1856-byte rows, a live window of ~45 MB: more than the SMs' shared memory
+    (8, 8, 128, 24576, 512, 30208),
+])
+def test_ring_rebase_two_leg_route_matches_oracle(shape):
+    """The ring rebase moves the live rows through shared memory in one pass
+    when it can; rows that are not 16-byte multiples and windows larger than
+    the SMs' shared memory take the two copy legs through the workspace.
+    Both shapes here take the two legs, across several rebases: the live rows
+    equal the oracle's bytes and decode matches the windowed oracle."""
+    Hq, Hkv, D, W, MT, N = shape
+    p = Pair(1, Hkv, D, Hq, max_t=MT, window=W, ring=True)
+    k = _randn(1, N, Hkv, D, seed=131)
+    v = _randn(1, N, Hkv, D, seed=132)
+    s = _randn(Hq, seed=133)
+    L, rebases, base0 = 0, 0, 0
+    while L < N:
+        T = min(MT, N - L)
+        p.append(k[:, L:L + T], v[:, L:L + T])
+        L += T
+        base = p.dev.bases()[0]
+        rebases += base != base0
+        base0 = base
+        if base != 0 and rebases <= 2:
+            assert_rows_equal(p.dev, p.ora, 0, max(0, L - W), L)
+    assert rebases >= 2
+    got, ref = p.decode(_randn(1, 1, Hq, D, seed=134), sinks=s)
+    assert_close(got, ref)
+    assert_rows_equal(p.dev, p.ora, 0, max(0, L - W), L)
+    assert p.dev.device_error() == 0
+
+
 @pytest.mark.parametrize("path", [(0, 0), (1, 0), (2, 16)], ids=["auto", "generic", "stream"])
 @pytest.mark.parametrize("shape", [
     # B, Hq, Hkv, D, lens, T, window, sinks

@@ -81,3 +81,32 @@ def test_noalloc_refuses_oversize_partials():
     out = c.decode(q)
     torch.cuda.synchronize()
     assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("name", ["ctx512", "ctx32k", "batch64", "swa_ring", "spec_verify"])
+def test_noalloc_fits_every_workload_at_full_size(name):
+    """Each of the five decode workloads at its full size (automatic kernel
+    choice, as benchmarked) fits the 16 MiB scratch, and the no-alloc decode
+    gives the bytes of the workspace decode."""
+    _need_gpu()
+    from quantized_kv_cache_08_gb300.inputs import workload
+    wl = workload(name)
+    lens = [2 * wl.window] if wl.ring else list(wl.lengths())
+    c = KVCache(wl.n_seq, wl.n_kv, wl.head_dim, wl.n_q, max_t=512,
+                max_rows=0 if wl.ring else max(lens) + wl.T, window=wl.window, ring=wl.ring)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    for b, L in enumerate(lens):
+        for t0 in range(0, L, 512):
+            n = min(512, L - t0)
+            k = torch.randn(1, n, wl.n_kv, wl.head_dim, generator=g, device="cuda")
+            v = torch.randn(1, n, wl.n_kv, wl.head_dim, generator=g, device="cuda")
+            c.append(k, v, seq_ids=[b])
+    q = torch.randn(wl.n_seq, wl.T, wl.n_q, wl.head_dim, generator=g, device="cuda")
+    if wl.q_dtype == "bf16":
+        q = q.to(torch.bfloat16)
+    sinks = torch.randn(wl.n_q, generator=g, device="cuda") if wl.sinks else None
+    ref = c.decode(q, sinks=sinks)
+    got = _noalloc(c, q, sinks)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+    assert c.device_error() == 0
