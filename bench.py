@@ -278,8 +278,9 @@ def measure(args, name, world, rank, local):
         k_new.append(kk.to(dev))
         v_new.append(vv.to(dev))
         qs.append(wl.q(r + 7 * rank, T=T).to(dev))
-    outs = [torch.empty(wl.n_seq, T, wl.n_q, wl.head_dim, dtype=torch.float32, device=dev)
-            for _ in range(R)]
+    # the layers' outputs side by side in one buffer: the step's result
+    out_all = torch.empty(R, wl.n_seq, T, wl.n_q, wl.head_dim, dtype=torch.float32, device=dev)
+    outs = list(out_all.unbind(0))
     accept0 = torch.zeros(wl.n_seq, dtype=torch.int32, device=dev)
 
     def rollback(c):
@@ -388,7 +389,7 @@ def measure(args, name, world, rank, local):
 
     # --- end to end through the public API: the step's inputs (K, V rows and
     # queries, in their own dtypes) in one pinned host buffer copied in with
-    # one copy, every output copied out
+    # one copy, the step's outputs (every layer's) copied out with one copy
     segs, off = [], 0
     for x in k_new + v_new + qs:
         nb = x.numel() * x.element_size()
@@ -401,15 +402,15 @@ def measure(args, name, world, rank, local):
         host_in[o:o + nb].copy_(x.reshape(-1).view(torch.uint8).cpu())
         ins.append(dev_in[o:o + nb].view(x.dtype).view(x.shape))
     dk, dv, dq = ins[:R], ins[R:2 * R], ins[2 * R:]
-    pin_o = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    pin_o = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
 
     def e2e_step():
         dev_in.copy_(host_in, non_blocking=True)
         for r, c in enumerate(caches):
             c.append(dk[r], dv[r])
             c.decode(dq[r], sinks=sinks_d, out=outs[r])
-            pin_o[r].copy_(outs[r], non_blocking=True)
             rollback(c)
+        pin_o.copy_(out_all, non_blocking=True)
 
     # eager: every call from Python, as a caller without graphs makes them
     for _ in range(args.warmup):
@@ -435,7 +436,7 @@ def measure(args, name, world, rank, local):
     e2e_ms = max_over_ranks(statistics.median(replay_ms(g_e2e) for _ in range(3)), world)
     sync_all()
     h2d = sum(nb for _, nb, _ in segs)
-    d2h = sum(x.numel() * x.element_size() for x in pin_o)
+    d2h = pin_o.numel() * pin_o.element_size()
     e2e_value = world * kv_bytes_step * args.steps / (e2e_ms * 1e-3) / 1e9
 
     extra = ""
@@ -469,7 +470,7 @@ def measure(args, name, world, rank, local):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4),
                 "how": "K steps of the public calls with their pinned-host copies (the step's K, V "
-                       "and queries in one buffer, each output back), captured as one CUDA graph and "
+                       "and queries in one buffer in, every layer's output in one buffer back), captured as one CUDA graph and "
                        "replayed; the whole step's time (copies, append, decode, rollback) divides the "
                        "decode's bytes",
                 "eager_value": round(world * kv_bytes_step * args.steps / (e2e_eager_ms * 1e-3) / 1e9, 2)},
@@ -578,6 +579,117 @@ def run_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------------------ ncu summaries
+
+_UNITS = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "ns": 1e-3, "nsecond": 1e-3, "us": 1.0,
+          "usecond": 1.0, "ms": 1e3, "msecond": 1e3, "s": 1e6, "second": 1e6}
+
+
+def _short_kernel(name):
+    """Kernel name without return type, namespaces and parameter list."""
+    name = re.sub(r"^void ", "", name).replace("<unnamed>", "anon").replace("unnamed>", "anon").replace("(anonymous namespace)", "anon")
+    depth, cut = 0, len(name)
+    for i, ch in enumerate(name):
+        if ch == "<":
+            depth += 1
+        elif ch == ">":
+            depth -= 1
+        elif ch == "(" and depth == 0:
+            cut = i
+            break
+    name = name[:cut]
+    return re.sub(r"^(?:[A-Za-z_]\w*::)+", "", name)
+
+
+def read_ncu_csv(path):
+    """Launches of an `ncu --csv --log-file` log: [(id, kernel, {metric: value})],
+    bytes in bytes and times in microseconds."""
+    import csv
+    with open(path) as fh:
+        lines = [ln for ln in fh if not ln.startswith("==")]
+    rows = list(csv.reader(lines))
+    hdr = next(i for i, r in enumerate(rows) if "Metric Name" in r)
+    cols = {name: j for j, name in enumerate(rows[hdr])}
+    launches = {}
+    for r in rows[hdr + 1:]:
+        if len(r) < len(cols):
+            continue
+        lid = int(r[cols["ID"]])
+        unit = r[cols["Metric Unit"]].strip().lower()
+        try:
+            v = float(r[cols["Metric Value"]].replace(",", "")) * _UNITS.get(unit, 1.0)
+        except ValueError:
+            continue
+        e = launches.setdefault(lid, (r[cols["Kernel Name"]], {}))
+        e[1][r[cols["Metric Name"]]] = v
+    return [(lid, k, m) for lid, (k, m) in sorted(launches.items())]
+
+
+def _decode_role(kernel):
+    if "merge" in kernel:
+        return "merge_kernel"
+    if "stream_kernel" in kernel or "split_kernel" in kernel:
+        return "split_kernel"
+    return None
+
+
+def record_ncu_traffic(args, path, how):
+    """Average DRAM bytes per launch of the decode's split and merge kernels in
+    an ncu log, written to profiles/traffic.json under this run's key, with
+    the kernel-source hash they belong to."""
+    wl = bench_workload(args)
+    fmt = args.kv_format
+    sums = {}
+    for _, kernel, m in read_ncu_csv(path):
+        role = _decode_role(kernel)
+        if role is None or "dram__bytes_read.sum" not in m:
+            continue
+        acc = sums.setdefault(role, [0, 0.0, 0.0, kernel])
+        acc[0] += 1
+        acc[1] += m["dram__bytes_read.sum"]
+        acc[2] += m.get("dram__bytes_write.sum", 0.0)
+    if "split_kernel" not in sums:
+        raise SystemExit(f"{path}: no split-kernel launch with dram__bytes_read.sum")
+    alg = sum(visible_rows(wl, L) for L in decode_lengths(wl)) * kv_bytes_per_row(wl, fmt)
+    key = traffic_key(wl.name, fmt, args)
+    rec = {"source_hash": kernel_source_hash(), "algorithmic_bytes_per_decode": alg, "how": how}
+    total = 0
+    for role, (n, rd, wr, kernel) in sums.items():
+        rec[role] = {"kernel": _short_kernel(kernel), "launches": n, "dram_bytes_read": int(round(rd / n)),
+                     "dram_bytes_write": int(round(wr / n))}
+        total += rec[role]["dram_bytes_read"] + rec[role]["dram_bytes_write"]
+    rec["dram_bytes_per_decode"] = total
+    out = os.path.join(ROOT, "profiles", "traffic.json")
+    d = {}
+    if os.path.exists(out):
+        with open(out) as fh:
+            d = json.load(fh)
+    d[key] = rec
+    with open(out, "w") as fh:
+        json.dump(d, fh, indent=1, sort_keys=True)
+        fh.write("\n")
+    return key, rec
+
+
+def launch_table(path):
+    """Markdown launch list of an ncu log of gpu__time_duration.sum: launches,
+    total and mean time and share per kernel."""
+    per = {}
+    for _, kernel, m in read_ncu_csv(path):
+        t = m.get("gpu__time_duration.sum")
+        if t is None:
+            continue
+        e = per.setdefault(_short_kernel(kernel), [0, 0.0])
+        e[0] += 1
+        e[1] += t
+    tot = sum(v[1] for v in per.values())
+    out = ["| kernel | launches | total µs | share | mean µs |", "|---|---|---|---|---|"]
+    for k, (n, t) in sorted(per.items(), key=lambda kv: -kv[1][1]):
+        out.append(f"| `{k}` | {n} | {t:.1f} | {100 * t / tot:.1f}% | {t / n:.2f} |")
+    out.append(f"| total | {sum(v[0] for v in per.values())} | {tot:.1f} | 100% | |")
+    return "\n".join(out)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -598,7 +710,22 @@ def main():
                     help="how each step rolls back to the snapshot: host lengths (kvq_truncate) or "
                          "accepted counts on the device (kvq_truncate_device)")
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--ncu-traffic", metavar="CSV",
+                    help="record the decode kernels' DRAM bytes per launch from an ncu --csv log "
+                         "(dram__bytes_read.sum, dram__bytes_write.sum) in profiles/traffic.json under "
+                         "this run's workload and options, then exit; --ncu-how gives the command")
+    ap.add_argument("--ncu-how", default="", help="the ncu command that wrote the --ncu-traffic log")
+    ap.add_argument("--ncu-launches", metavar="CSV",
+                    help="print the launch list (launches, time, share per kernel) of an ncu --csv log "
+                         "of gpu__time_duration.sum as a markdown table, then exit")
     args = ap.parse_args()
+    if args.ncu_traffic:
+        key, rec = record_ncu_traffic(args, args.ncu_traffic, args.ncu_how)
+        print(json.dumps({key: rec}, indent=1))
+        return
+    if args.ncu_launches:
+        print(launch_table(args.ncu_launches))
+        return
     if args.warmup < 3:
         args.warmup = 3
     if not 0 <= args.t <= 512:

@@ -147,7 +147,7 @@ WsLayout ws_layout(const kvq_config* c, const Geometry& g) {
     w.part_o = 0;
     w.part_ml = round_up(w.part_o + recs * c->head_dim * sizeof(float), 256);
     w.plan = round_up(w.part_ml + recs * 2 * sizeof(float), 256);
-    w.scratch = round_up(w.plan + (c->n_seq + 2 + kStreamMaxGrid) * sizeof(int), 256);
+    w.scratch = round_up(w.plan + (c->n_seq + 1) * sizeof(int), 256);
     w.total = w.scratch + (c->ring ? round_up((size_t)g.rows * (g.k_tok + g.v_tok), 256) : 0);
     return w;
 }
@@ -445,7 +445,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
             if (scratch) {
                 const size_t o_ml = round_up(recs * D * sizeof(float), 256);
                 const size_t o_plan = round_up(o_ml + recs * 2 * sizeof(float), 256);
-                const size_t need = o_plan + (B + 2 + p.G) * sizeof(int);
+                const size_t need = o_plan + (B + 1) * sizeof(int);
                 if (need > scratch_bytes)
                     return fail(KVQ_ERANGE,
                                 "this decode needs %zu bytes of scratch, the no-alloc entry point holds %zu", need,

@@ -489,8 +489,8 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
     __shared__ int s_wsum[kWarps];
     __shared__ __align__(8) uint64_t s_pair[kWarps];   // per unit of two row slices: sums in, sums read
 
-    // ---- visible rows of every sequence from the device counters, prefix sums
     if (tid == 0) s_abort = 0;
+    // ---- visible rows of every sequence from the device counters, prefix sums
     int v2[2] = {0, 0};
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -547,14 +547,9 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         walk_init(s_walk, tb, B, R, x0, x1);
     }
-    // the plan for the merge: the prefix of visible rows, then every CTA's
-    // range start (and the end of the work space after the last)
+    // the plan for the merge: the prefix of visible rows
     if (blockIdx.x == 0)
         for (int b = tid; b <= B; b += kThreads) p.plan[b] = tb.pre[b];
-    if (tid == 0) {
-        p.plan[B + 1 + blockIdx.x] = (int)x0;
-        if (blockIdx.x == p.G - 1) p.plan[B + 1 + p.G] = (int)x1;
-    }
     __syncthreads();
     // let the merge grid launch; it waits for this grid before reading partials
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -573,16 +568,13 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
         tma_rows(kst0 + (uint32_t)s * L.kstage, &kmap, y, bar);
         tma_rows(vst0 + (uint32_t)s * L.vstage, &vmap, y, bar);
     };
-    // ---- the first NS tiles
+    // ---- the first tile now; the next NS - 1 once warp 0 has its queries, so
+    // that the query loads of every CTA do not queue behind the copy burst
     if (tid == 0) {
-        for (int j = 0; j < NS; ++j) {
-            const int4 tile = walk_take(s_walk, tb, B);
-            if (tile.x == -2) break;
-            s_tinfo[j] = tile;
-            arm[j] = 1;
-            issue(j, tile);
-            if (tile.x < 0) break;
-        }
+        const int4 tile = walk_take(s_walk, tb, B);     // a tile, or the end marker
+        s_tinfo[0] = tile;
+        arm[0] = 1;
+        issue(0, tile);
     }
     __syncthreads();
     if (warp >= p.NA) return;
@@ -649,9 +641,19 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
         for (int jj = 0; jj < QPL; ++jj) sq[jj] = STw[4 + kp * QPL + jj];
     };
     {
-        // the first fragment's queries load while the first tiles are in flight
+        // the first fragment's queries load while the first tile is in flight
         const int4 t0 = s_tinfo[0];
         if (t0.x >= 0) begin_fragment(t0.x, t0.y);
+        if (tid == 0 && t0.x >= 0) {
+            for (int j = 1; j < NS; ++j) {
+                const int4 tile = walk_take(s_walk, tb, B);
+                if (tile.x == -2) break;
+                s_tinfo[j] = tile;
+                arm[j] = 1;
+                issue(j, tile);
+                if (tile.x < 0) break;
+            }
+        }
     }
 
     // tile j sits in stage st = j mod NS, use u = j div NS of it (phase parity
@@ -923,8 +925,8 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
 //   out = sum o_r 2^(m_r - M) / L.
 // The records of (b, q) are those of the CTAs whose ranges meet the rows
 // [xa, xb) of key (slice of q, b): CTA c covers [c W / G, (c + 1) W / G), so
-// the CTA holding row x is ((x + 1) G - 1) / W; the split kernel also writes
-// the range starts, which tell an empty range (no record) apart.  A CTA has 16 warps; WPQ
+// the CTA holding row x is ((x + 1) G - 1) / W, and with fewer rows W than
+// CTAs a range may be empty (no record).  A CTA has 16 warps; WPQ
 // warps share one (sequence, query, chunk of DC = 32 * VPL dims), each
 // folding every WPQ-th record with U records' loads in flight, and their
 // states meet in shared memory.
@@ -947,7 +949,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_stream_kernel(const Merge
         b = (int)(r / p.Qtot);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int* starts = p.plan + p.B + 1;            // CTA c covers [starts[c], starts[c + 1])
     const int R = p.plan[p.B];
     const int t = qg / p.Hq, h = qg - t * p.Hq;
     const int qi = t * p.hpk + (h % p.hpk);
@@ -959,14 +960,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_stream_kernel(const Merge
     const int xa = qs * R + p.plan[b];
     const int xb = xa + (p.plan[b + 1] - p.plan[b]);
     int c_lo = 0, nrec = 0;
+    const long long W = (long long)R * p.nqs;
     if (live && xb > xa) {
         // the CTAs holding rows xa and xb - 1: CTA c starts at floor(c W / G),
         // so the CTA of row x is ((x + 1) G - 1) / W
-        const long long W = (long long)R * p.nqs;
         c_lo = (int)(((long long)(xa + 1) * p.G - 1) / W);
         const int c_hi = (int)(((long long)xb * p.G - 1) / W);
         nrec = c_hi - c_lo + 1;
     }
+    // with fewer rows than CTAs some ranges are empty and wrote no record
+    const bool some_empty = W < p.G;
     const int dim0 = ch * DC + lane * VPL;
     float M = kNegInf, Ls = 0.f, acc[VPL];
 #pragma unroll
@@ -980,7 +983,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_stream_kernel(const Merge
             long long rec = 0;
             if (ok) {
                 const int c = c_lo + r;
-                ok = starts[c + 1] > starts[c];               // an empty CTA range wrote nothing
+                if (some_empty) ok = W * (c + 1) / p.G > W * c / p.G;
                 rec = (long long)(c + key) * QS + qloc;
             }
             const float2 mlv = ok ? *reinterpret_cast<const float2*>(p.part_ml + rec * 2) : make_float2(kNegInf, 0.f);

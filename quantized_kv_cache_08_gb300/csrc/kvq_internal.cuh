@@ -134,7 +134,7 @@ struct StreamParams {
     int qbits;                     // 16 or 24: query quantisation
     float* part_o;                 // [slot][4 Hkv QPS][D]: the slice's queries, unit-major
     float* part_ml;                // [slot][4 Hkv QPS][2]  (max in log2 units, sum)
-    int* plan;                     // [B+1] prefix of visible rows, then [G+1] CTA range starts
+    int* plan;                     // [B+1] prefix of visible rows, written by CTA 0
 };
 
 struct StreamLayout {
