@@ -114,6 +114,23 @@ __device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, volatil
 
 // ------------------------------------------------------------ the walk
 
+// floor(W c / G) for 0 <= W < 2^31 and 0 <= c <= G <= 2^16, in 32-bit
+// arithmetic: W = q G + r gives q c + floor(r c / G)
+__device__ __forceinline__ int range_bound(int W, int c, int G) {
+    const unsigned q = (unsigned)W / (unsigned)G, r = (unsigned)W - q * (unsigned)G;
+    return (int)(q * (unsigned)c + (r * (unsigned)c) / (unsigned)G);
+}
+
+// floor(n / d) for 0 <= n < 2^47 and 0 < d < 2^31 when the quotient is below
+// 2^16: a float estimate, then exact integer corrections
+__device__ __forceinline__ int small_quotient(long long n, long long d) {
+    int q = (int)((float)n / (float)d);
+    q = max(q, 0);
+    while ((long long)q * d > n) --q;
+    while ((long long)(q + 1) * d <= n) ++q;
+    return q;
+}
+
 // Cursor over the CTA's range of the work space: the current fragment is
 // key (qs, b), logical rows [row, end) with `start` its first row, and xrem
 // rows of the range follow it.  Only one thread at a time touches it.
@@ -147,7 +164,7 @@ __device__ __forceinline__ void walk_init(Walk* w, const Tables& t, int B, long 
         w->b = -1;
         return;
     }
-    const int qs = (int)(x0 / R);
+    const int qs = (int)((unsigned)x0 / (unsigned)R);        // both below 2^31
     const int xr = (int)(x0 - (long long)qs * R);
     int lo = 0, hi = B;                            // largest b with pre[b] <= xr
     while (hi - lo > 1) {
@@ -204,11 +221,12 @@ __device__ __forceinline__ int4 walk_take(Walk* w, const Tables& t, int B) {
 // 32 rows from row y of a plane by one 2-D TMA tensor copy.  The map's element
 // is 8 bytes and its box row is the padded stage row: the part past the token
 // row lies outside the tensor and is filled with zeros, so rows land at the
-// padded stride.
+// padded stride.  The rows are read once per decode: evict-first in L2.
 __device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap* map, int y, uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(bar), "l"(evict_first_policy())
         : "memory");
 }
 
@@ -536,8 +554,8 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
     }
     __syncthreads();
     const long long R = tb.pre[B];
-    const long long Wtot = R * p.nqs;
-    const long long x0 = Wtot * blockIdx.x / p.G, x1 = Wtot * (blockIdx.x + 1) / p.G;
+    const long long Wtot = R * p.nqs;                // below 2^31 (checked on the host)
+    const long long x0 = range_bound((int)Wtot, blockIdx.x, p.G), x1 = range_bound((int)Wtot, blockIdx.x + 1, p.G);
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
@@ -964,8 +982,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_stream_kernel(const Merge
     if (live && xb > xa) {
         // the CTAs holding rows xa and xb - 1: CTA c starts at floor(c W / G),
         // so the CTA of row x is ((x + 1) G - 1) / W
-        c_lo = (int)(((long long)(xa + 1) * p.G - 1) / W);
-        const int c_hi = (int)(((long long)xb * p.G - 1) / W);
+        c_lo = small_quotient((long long)(xa + 1) * p.G - 1, W);
+        const int c_hi = small_quotient((long long)xb * p.G - 1, W);
         nrec = c_hi - c_lo + 1;
     }
     // with fewer rows than CTAs some ranges are empty and wrote no record
@@ -983,7 +1001,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_stream_kernel(const Merge
             long long rec = 0;
             if (ok) {
                 const int c = c_lo + r;
-                if (some_empty) ok = W * (c + 1) / p.G > W * c / p.G;
+                if (some_empty) ok = range_bound((int)W, c + 1, p.G) > range_bound((int)W, c, p.G);
                 rec = (long long)(c + key) * QS + qloc;
             }
             const float2 mlv = ok ? *reinterpret_cast<const float2*>(p.part_ml + rec * 2) : make_float2(kNegInf, 0.f);
