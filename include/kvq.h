@@ -187,14 +187,13 @@ kvq_status kvq_decode(kvq_cache* cache, const void* q, kvq_dtype dtype, int T,
  * kvq_decode (the same kernels run on the same split plan), but the split
  * partials and the plan live in a file-scope device array of
  * KVQ_NOALLOC_SCRATCH_BYTES (16 MiB) inside the library: the call allocates
- * nothing.  The decode needs R records of (head_dim + 2) * 4 bytes plus its
- * plan.  On the stream-K kernel R = (G + nqs * n_seq) * 4 * Hkv * QPS and the
- * plan is n_seq + 1 ints, where G <= 256 is the CTA count (one per SM at
- * most), u = ceil(hpk * T / 4) four-query units per KV head (hpk =
+ * nothing.  The decode needs R records of (head_dim + 2) * 4 bytes.  On the
+ * stream-K kernel R = (G + nqs * n_seq) * 4 * Hkv * QPS, where G <= 256 is
+ * the CTA count (one per SM at most), u = ceil(hpk * T / 4) four-query units per KV head (hpk =
  * n_q_heads / Hkv), QPS = max(1, min(u, 16 / Hkv)) and nqs = ceil(u / QPS):
  * 64 sequences with 8 KV heads, 32 Q heads and T = 1 need about 3.6 MB on 152
  * SMs.  On the generic kernel R = n_seq * ceil(max visible rows / split rows)
- * * n_q_heads * T, with the same plan.  A call that needs more
+ * * n_q_heads * T, plus a plan of n_seq + 1 ints.  A call that needs more
  * returns KVQ_ERANGE (nothing launched) and says how much.  Nothing in the
  * array has to start at zero: every byte read was written earlier in the
  * same call.  The array's address is resolved (cudaGetSymbolAddress, with the

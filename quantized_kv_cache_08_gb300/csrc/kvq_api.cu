@@ -444,26 +444,26 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
             const size_t recs = stream_records(&c->cfg, sh, p.G);
             if (scratch) {
                 const size_t o_ml = round_up(recs * D * sizeof(float), 256);
-                const size_t o_plan = round_up(o_ml + recs * 2 * sizeof(float), 256);
-                const size_t need = o_plan + (B + 1) * sizeof(int);
+                const size_t need = o_ml + recs * 2 * sizeof(float);
                 if (need > scratch_bytes)
                     return fail(KVQ_ERANGE,
                                 "this decode needs %zu bytes of scratch, the no-alloc entry point holds %zu", need,
                                 scratch_bytes);
                 p.part_o = reinterpret_cast<float*>(scratch);
                 p.part_ml = reinterpret_cast<float*>(scratch + o_ml);
-                p.plan = reinterpret_cast<int*>(scratch + o_plan);
             } else {
                 p.part_o = reinterpret_cast<float*>(c->ws + c->off_part_o);
                 p.part_ml = reinterpret_cast<float*>(c->ws + c->off_part_ml);
-                p.plan = reinterpret_cast<int*>(c->ws + c->off_plan);
             }
             cudaError_t e = launch_split_stream(p, c->kmap, c->vmap, s);
             if (e != cudaSuccess) return cuda_fail(e, "decode split kernel");
             MergeStreamParams m;
             m.part_o = p.part_o;
             m.part_ml = p.part_ml;
-            m.plan = p.plan;
+            m.len_d = c->len_d;
+            m.base_d = c->base_d;
+            m.window = c->cfg.window;
+            m.max_rows = c->rows;
             m.sinks = sinks;
             m.out = out;
             m.B = B;

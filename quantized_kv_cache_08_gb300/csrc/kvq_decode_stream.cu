@@ -565,9 +565,6 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         walk_init(s_walk, tb, B, R, x0, x1);
     }
-    // the plan for the merge: the prefix of visible rows
-    if (blockIdx.x == 0)
-        for (int b = tid; b <= B; b += kThreads) p.plan[b] = tb.pre[b];
     __syncthreads();
     // let the merge grid launch; it waits for this grid before reading partials
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -944,7 +941,11 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
 // The records of (b, q) are those of the CTAs whose ranges meet the rows
 // [xa, xb) of key (slice of q, b): CTA c covers [c W / G, (c + 1) W / G), so
 // the CTA holding row x is ((x + 1) G - 1) / W, and with fewer rows W than
-// CTAs a range may be empty (no record).  A CTA has 16 warps; WPQ
+// CTAs a range may be empty (no record).  The rows [xa, xb) come from the
+// prefix of visible rows, which each merge CTA derives from the counters by
+// the split kernel's rule while the split grid still runs (the merge is its
+// programmatic dependent; the counters do not change until both end), so the
+// only wait on the split is for the records.  A CTA has 16 warps; WPQ
 // warps share one (sequence, query, chunk of DC = 32 * VPL dims), each
 // folding every WPQ-th record with U records' loads in flight, and their
 // states meet in shared memory.
@@ -966,8 +967,49 @@ __global__ void __launch_bounds__(kMergeThreads) merge_stream_kernel(const Merge
         qg = (int)(r % p.Qtot);
         b = (int)(r / p.Qtot);
     }
+    // the prefix of visible rows, by the split kernel's rule, while the split
+    // grid still runs: the counters are final once it has started
+    int* spre = reinterpret_cast<int*>(msm + kMergeWarps * (2 + DC));   // [B + 1]
+    {
+        __shared__ int s_wsum[kMergeWarps];
+        int v2[2] = {0, 0};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int bb = 2 * (int)threadIdx.x + e;
+            if (bb < p.B) {
+                const int len = p.len_d[bb], base = p.base_d[bb];
+                const int lo = p.window > 0 ? max(0, len - p.T + 1 - p.window) : 0;
+                const bool bad = len < p.T || base < 0 || len - base > p.max_rows || lo < base;
+                v2[e] = bad ? 0 : len - lo;
+            }
+        }
+        const int own = v2[0] + v2[1];
+        int x = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = lane < kMergeWarps ? s_wsum[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            if (lane < kMergeWarps) s_wsum[lane] = w;
+        }
+        __syncthreads();
+        const int excl = x - own + (warp > 0 ? s_wsum[warp - 1] : 0);
+        if (2 * (int)threadIdx.x < p.B) spre[2 * threadIdx.x] = excl;
+        if (2 * (int)threadIdx.x + 1 < p.B) spre[2 * threadIdx.x + 1] = excl + v2[0];
+        if (threadIdx.x == 0) spre[p.B] = s_wsum[kMergeWarps - 1];
+        __syncthreads();
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int R = p.plan[p.B];
+    const int R = spre[p.B];
     const int t = qg / p.Hq, h = qg - t * p.Hq;
     const int qi = t * p.hpk + (h % p.hpk);
     const int qs = (qi >> 2) / p.QPS;
@@ -975,8 +1017,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_stream_kernel(const Merge
     const int QS = 4 * (p.Hq / p.hpk) * p.QPS;
     const int qloc = ((h / p.hpk) * p.QPS + (qi >> 2) - qs * p.QPS) * 4 + (qi & 3);
     const int key = qs * p.B + b;
-    const int xa = qs * R + p.plan[b];
-    const int xb = xa + (p.plan[b + 1] - p.plan[b]);
+    const int xa = qs * R + spre[b];
+    const int xb = xa + (spre[b + 1] - spre[b]);
     int c_lo = 0, nrec = 0;
     const long long W = (long long)R * p.nqs;
     if (live && xb > xa) {
@@ -1088,7 +1130,7 @@ template <int VPL, int U>
 cudaError_t launch_merge_stream_t(const MergeStreamParams& p, cudaStream_t s) {
     const int PPC = kMergeWarps / p.WPQ;
     const long long npairs = (long long)p.B * p.Qtot * (p.D / (32 * VPL));
-    const size_t smem = (size_t)kMergeWarps * (2 + 32 * VPL) * sizeof(float);
+    const size_t smem = (size_t)kMergeWarps * (2 + 32 * VPL) * sizeof(float) + (size_t)(p.B + 1) * sizeof(int);
     auto fn = merge_stream_kernel<VPL, U>;
     static std::atomic<unsigned long long> attrs{0};
     cudaError_t e = kernel_attrs_once(fn, attrs, true);

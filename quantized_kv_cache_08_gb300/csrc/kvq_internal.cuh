@@ -134,7 +134,6 @@ struct StreamParams {
     int qbits;                     // 16 or 24: query quantisation
     float* part_o;                 // [slot][4 Hkv QPS][D]: the slice's queries, unit-major
     float* part_ml;                // [slot][4 Hkv QPS][2]  (max in log2 units, sum)
-    int* plan;                     // [B+1] prefix of visible rows, written by CTA 0
 };
 
 struct StreamLayout {
@@ -184,7 +183,9 @@ __host__ __device__ inline StreamLayout stream_layout(const StreamParams& p) {
 struct MergeStreamParams {
     const float* part_o;
     const float* part_ml;
-    const int* plan;               // [B+1] prefix of visible rows, [G+1] CTA range starts
+    const int* len_d;              // the counters: the merge derives the visible
+    const int* base_d;             // rows of each sequence as the split kernel does
+    int window, max_rows;
     const float* sinks;            // [Hq] or null
     float* out;                    // [B][T][Hq][D]
     int B, T, Hq, hpk, D, Qtot, QPS, nqs, G;
