@@ -437,6 +437,14 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         const long long work = total_vis * sh.nqs;
         p.G = (int)std::max(1LL, std::min<long long>((work + kStreamRows - 1) / kStreamRows,
                                                      std::min(kStreamCtasPerSm * c->num_sms, kStreamMaxGrid)));
+        // two row slices per tile pay off in the steady state (twice the warps
+        // hide more latency); with few tiles per CTA one slice wins (half the
+        // query preparation, no pair hand-over at a record): measured on
+        // GB300 the turn is near 16 tiles per CTA
+        if (p.RS == 2 && work <= kStreamShortTiles * kStreamRows * (long long)p.G) {
+            p.RS = 1;
+            p.NA = Hkv * sh.QPS;
+        }
         const int smem_max = stream_max_smem();
         p.NS = 3;
         while (p.NS > 2 && stream_layout(p).total > (size_t)smem_max) --p.NS;

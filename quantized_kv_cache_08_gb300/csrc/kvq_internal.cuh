@@ -110,6 +110,7 @@ constexpr int kStreamRows = 32;         // token rows per tile
 constexpr int kStreamCtasPerSm = 1;
 constexpr int kStreamMaxB = 1024;       // sequences the per-CTA tables hold
 constexpr int kStreamMaxGrid = 256;     // most CTAs a decode may use (record slots are sized by it)
+constexpr int kStreamShortTiles = 16;   // at most this many tiles per CTA: one row slice per tile
 
 struct StreamParams {
     const uint8_t* k_plane;
