@@ -159,6 +159,9 @@ __device__ __forceinline__ void append_block(const AppendParams& p, const SeqIds
 // completion counter once its warps have read len_d, and the last one, which
 // resets the counter for the next launch, commits.
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p, SeqIds ids, long long n_work) {
+    // a decode launched next may start now: it waits for this grid (and its
+    // writes) before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (w < n_work) append_block(p, ids, w, lane);

@@ -508,6 +508,9 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
     __shared__ __align__(8) uint64_t s_pair[kWarps];   // per unit of two row slices: sums in, sums read
 
     if (tid == 0) s_abort = 0;
+    // launched as a programmatic dependent of the kernel before it (an append
+    // lets it start early): nothing that kernel may write is read before this
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // ---- visible rows of every sequence from the device counters, prefix sums
     int v2[2] = {0, 0};
 #pragma unroll
@@ -1122,7 +1125,18 @@ cudaError_t launch_stream_t(const StreamParams& p, const CUtensorMap& kmap, cons
     static std::atomic<unsigned long long> attrs{0};
     cudaError_t e = kernel_attrs_once(fn, attrs, true);
     if (e != cudaSuccess) return e;
-    fn<<<p.G, kThreads, smem, s>>>(p, kmap, vmap);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.G, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fn, p, kmap, vmap);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
