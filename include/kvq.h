@@ -269,16 +269,17 @@ kvq_status kvq_read_device_error(kvq_cache* cache, int* err, void* stream);
 /* Choose the decode kernel: path 0 = automatic (the stream-K kernel whenever
  * it allows the cache and the call, else the generic split kernel),
  * 1 = generic, 2 = stream-K (KVQ_EUNSUPPORTED at decode time if it does not
- * allow them).  The stream-K kernel needs the q8_0/q5_1 formats, K and V
- * token rows that are 16-byte multiples (n_kv_heads * head_dim a multiple of
- * 256), head_dim 64, 128 or 256, n_kv_heads <= 16, n_seq <= 1024 and its
- * tiles within shared memory; FP8 E4M3 caches always decode on the generic
- * kernel.  query_bits (0 = 16, or 16, or 24): the stream-K kernel quantises
+ * allow them).  The stream-K kernel needs K and V token rows that are
+ * 16-byte multiples (q8_0/q5_1: n_kv_heads * head_dim a multiple of 256;
+ * E4M3: of 16) and at most 2048 bytes, head_dim 64, 128 or 256,
+ * n_kv_heads <= 16, n_seq <= 1024 and its tiles within shared memory.
+ * query_bits (0 = 16, or 16, or 24): on q8_0 K the stream-K kernel quantises
  * each pre-scaled query element per 32-element block to this many bits
  * against the block's largest magnitude and multiplies it with the int8 K
  * codes in integer dot products; 16 bits adds an error below 1e-4 to the
  * attention output on unit-variance data, 24 bits is at the level of fp32
- * rounding and costs half again as many dot products. */
+ * rounding and costs half again as many dot products.  With E4M3 K the
+ * queries stay f32 and query_bits does not apply. */
 kvq_status kvq_set_decode_path(kvq_cache* cache, int path, int query_bits);
 
 /* Score soft-capping for later decodes ("Struct LayerKvCache": the softcap

@@ -112,7 +112,7 @@ struct StreamShape {
 StreamShape stream_shape(const kvq_config* c, const Geometry& g, int hpk, int T) {
     StreamShape sh{false, 1, 1, 1};
     const int NBH = c->head_dim / 32;
-    if (g.fp8 || g.k_tok % 16 || g.v_tok % 16 || !(NBH == 2 || NBH == 4 || NBH == 8) || c->n_seq > kStreamMaxB ||
+    if (g.k_tok % 16 || g.v_tok % 16 || !(NBH == 2 || NBH == 4 || NBH == 8) || c->n_seq > kStreamMaxB ||
         c->n_kv_heads > kStreamThreads / 32)
         return sh;
     const int nQG = (hpk * T + 3) / 4;
@@ -243,7 +243,7 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* 
     c->Sv = (uint32_t)g.v_tok;
     if (rows16)
         c->Sv += (uint32_t)((64 - g.v_tok % 128 + 128) % 128);
-    c->smap_ok = !g.fp8 && rows16 &&
+    c->smap_ok = rows16 &&
                  make_stream_map(&c->kmap, k_plane, g.k_tok, (int)c->Sk, (long long)cfg->n_seq * g.rows) &&
                  make_stream_map(&c->vmap, v_plane, g.v_tok, (int)c->Sv, (long long)cfg->n_seq * g.rows);
     c->path = 0;
@@ -399,7 +399,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
     const float cap_b = c->softcap > 0.f ? c->softcap * 1.4426950408889634f : 0.f;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    // ---- the stream-K kernel: q8_0 / q5_1, 16-byte token rows, head_dim 64, 128 or 256
+    // ---- the stream-K kernel: 16-byte token rows, head_dim 64, 128 or 256
     Geometry g{c->kb, c->k_tok, c->v_tok, c->rows, c->max_vis, c->fp8};
     const StreamShape sh = stream_shape(&c->cfg, g, hpk, T);
     if (c->path != 1 && sh.ok && c->smap_ok) {
@@ -431,6 +431,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         p.NA = Hkv * sh.QPS * sh.RS;
         p.Qtot = n_q_heads * T;
         p.qbits = c->qbits;
+        p.fp8 = c->fp8 ? 1 : 0;
         p.Sk = c->Sk;
         p.Sv = c->Sv;
         // CTAs: one per SM, fewer when there are fewer 32-row tiles of work
@@ -498,8 +499,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         }
     }
     if (c->path == 2)
-        return fail(KVQ_EUNSUPPORTED, c->fp8 ? "the stream-K decode reads q8_0/q5_1 only (use path 0 or 1)"
-                                             : "the stream-K decode does not support this geometry");
+        return fail(KVQ_EUNSUPPORTED, "the stream-K decode does not support this geometry");
 
     // ---- the generic split kernel
     const int QC = Q <= 4 ? 4 : 8;

@@ -1,7 +1,7 @@
-// Stream-K split decode for q8_0 / q5_1 caches whose token rows are 16-byte
-// multiples.  Same semantics as the generic split kernel (kvq_decode.cu):
-// cortiq-engine "Struct LayerKvCache" fn attend_group_upto (window, causal
-// upto, sinks, GQA) over memra-engine "Struct KvLayer" q8_0 / q5_1 rows.
+// Stream-K split decode for q8_0 / q5_1 and FP8 E4M3 caches whose token rows
+// are 16-byte multiples.  Same semantics as the generic split kernel
+// (kvq_decode.cu): cortiq-engine "Struct LayerKvCache" fn attend_group_upto
+// (window, causal upto, sinks, GQA) over memra-engine "Struct KvLayer" rows.
 //
 // Work.  The visible rows of all sequences, repeated once per query slice,
 // form one work space of W rows; CTA c takes rows [c W / G, (c + 1) W / G),
@@ -41,7 +41,13 @@
 // of its half block with byte arithmetic, places each in the mantissa of 0.5
 // (value 0.5 + u/256), so v_hat = 256 d F + (m - 128 d), and accumulates
 // o += (256 p d) F with packed FMAs and sum p (m - 128 d) per block.
+// E4M3 rows (template flag F8): the queries stay f32; each code word of K
+// and V becomes four exact floats (an E4M3 pair converts to a half pair, then
+// to floats) and both phases multiply with packed FMAs; a V lane takes 16
+// contiguous dims.
 #include "kvq_device.cuh"
+
+#include <cuda_fp8.h>
 
 #include <type_traits>
 
@@ -475,9 +481,101 @@ __device__ __forceinline__ void v_row(const uint8_t* vb, int h, uint32_t sel_lo,
     }
 }
 
+// ------------------------------------------------------------ FP8 E4M3 rows
+
+// Two E4M3 bytes (element order: low byte first) as two floats, exactly.
+__device__ __forceinline__ float2 e4m3x2_float2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// The 4 queries of unit (g, qg) of sequence b, pre-scaled (scale * log2 e)
+// and kept as f32: Wf[block][word of 4 codes][query][4], so a lane reads the
+// 4 values of a code word for its queries with one 16-byte load each.
+template <int NBH>
+__device__ __forceinline__ void prep_queries_f8(const StreamParams& p, int b, int g, int qg, float* Wf, float* SQ,
+                                                int lane) {
+    constexpr int D = NBH * 32;
+    constexpr int PL = D / 8;
+    const int n = lane >> 3, c8 = lane & 7;
+    const int qi = 4 * qg + n;
+    const bool valid = qi < p.Qh;
+    const int t = valid ? qi / p.hpk : 0, hr = valid ? qi - t * p.hpk : 0;
+    const int h = g * p.hpk + hr;
+    const long long src = ((long long)(b * p.T + t) * p.Hq + h) * D + c8 * PL;
+#pragma unroll
+    for (int k = 0; k < PL; k += 4) {
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (valid) {
+            if (p.q_bf16) {
+                const uint2 r = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.q) + src + k);
+                x[0] = __uint_as_float(r.x << 16);
+                x[1] = __uint_as_float(r.x & 0xffff0000u);
+                x[2] = __uint_as_float(r.y << 16);
+                x[3] = __uint_as_float(r.y & 0xffff0000u);
+            } else {
+                const float4 a = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.q) + src + k);
+                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+            }
+        }
+        const int d0 = c8 * PL + k;
+        const int i = d0 >> 5, w = (d0 & 31) >> 2;
+        *reinterpret_cast<float4*>(Wf + ((i * 8 + w) * 4 + n) * 4) =
+            make_float4(x[0] * p.qscale, x[1] * p.qscale, x[2] * p.qscale, x[3] * p.qscale);
+    }
+    if (c8 == 0) SQ[n] = 1.f;
+    __syncwarp();
+}
+
+// Scores of one E4M3 head row (D bytes at kc) for the lane's QPL queries:
+// each code word becomes 4 floats, multiplied into two partial sums per query
+// with packed FMAs.
+template <int NBH, int QPL>
+__device__ __forceinline__ void head_scores_f8(const uint4* __restrict__ kc, const float* __restrict__ qw,
+                                               float (&s)[QPL]) {
+    float2 acc[QPL];
+#pragma unroll
+    for (int j = 0; j < QPL; ++j) acc[j] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < NBH; ++i) {
+        const uint4 c0 = kc[2 * i], c1 = kc[2 * i + 1];
+        const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const float2 k01 = e4m3x2_float2(wv[w]), k23 = e4m3x2_float2(wv[w] >> 16);
+#pragma unroll
+            for (int j = 0; j < QPL; ++j) {
+                const float4 q4 = *reinterpret_cast<const float4*>(qw + ((i * 8 + w) * 4 + j) * 4);
+                acc[j] = __ffma2_rn(k01, make_float2(q4.x, q4.y), acc[j]);
+                acc[j] = __ffma2_rn(k23, make_float2(q4.z, q4.w), acc[j]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < QPL; ++j) s[j] = acc[j].x + acc[j].y;
+}
+
+// One staged E4M3 row for a V lane: its 16 contiguous dims, weighted by the
+// row's 4 probabilities p4 (256 p); o2[n][k] holds dims 2k, 2k + 1.
+__device__ __forceinline__ void v_row_f8(const uint8_t* vb, const float4 p4, float2 (&o2)[4][8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(vb);
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float2 fa = e4m3x2_float2(wv[c]), fb = e4m3x2_float2(wv[c] >> 16);
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            const float2 t2 = make_float2(pr[n], pr[n]);
+            o2[n][2 * c] = __ffma2_rn(t2, fa, o2[n][2 * c]);
+            o2[n][2 * c + 1] = __ffma2_rn(t2, fb, o2[n][2 * c + 1]);
+        }
+    }
+}
+
 // ------------------------------------------------------------ the kernel
 
-template <int NBH, int KP, int NQB>
+template <int NBH, int KP, int NQB, bool F8>
 __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(const StreamParams p,
                                                               const __grid_constant__ CUtensorMap kmap,
                                                               const __grid_constant__ CUtensorMap vmap) {
@@ -613,13 +711,16 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
     // K-phase lane: row kr of the warp's slice, part kp (queries kp*QPL..)
     const int kr = lane / KP, kp = lane - kr * KP;
     const int trow = rs * RW + kr;                  // tile row of this K lane
-    const int hb0 = 34 * NBH * g;                   // byte of the head's first K block in a row
+    // byte of the head's first K block in a row (q8_0: 34 B blocks; E4M3: D B)
+    const int hb0 = F8 ? D * g : 34 * NBH * g;
     const int ph = hb0 & 15;
     const uint32_t k_lane_off = (uint32_t)L.kst + (uint32_t)trow * p.Sk + (uint32_t)(hb0 - ph);
     // V-phase lane: row group vg, half block vh of block vi
     const int vg = lane / VH, vhb = lane - vg * VH;
     const int vi = vhb >> 1, vh = vhb & 1;
-    const uint32_t v_lane_off = (uint32_t)L.vst + (uint32_t)(rs * RW + vg) * p.Sv + (uint32_t)(24 * (NBH * g + vi));
+    // q5_1: half block vh of block vi (24 B blocks); E4M3: 16 contiguous dims
+    const uint32_t v_lane_off = (uint32_t)L.vst + (uint32_t)(rs * RW + vg) * p.Sv +
+                                (uint32_t)(F8 ? D * g + 16 * vhb : 24 * (NBH * g + vi));
     const uint32_t v_step = (uint32_t)RG * p.Sv;
 
     float lsum[QPL], sq[QPL], pm[4];
@@ -642,6 +743,9 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
     auto begin_fragment = [&](int b, int qs) {
         key = b * 65536 + qs;
         const int qg = qs * p.QPS + qgl;
+        if constexpr (F8)
+            prep_queries_f8<NBH>(p, b, g, qg, reinterpret_cast<float*>(smem + w_off), STw + 4, lane);
+        else
         prep_queries<NBH, NQB>(p, b, g, qg, reinterpret_cast<uint32_t*>(smem + w_off), smem + lw_off, STw + 4,
                                lane);
         if (lane < 4) {
@@ -691,7 +795,10 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
         for (int jj = 0; jj < QPL; ++jj) sc[jj] = 0.f;
         if (full_tile || trow < nr) {
             const uint4* kc = reinterpret_cast<const uint4*>(smem + k_lane_off + (uint32_t)st * L.kstage);
-            head_scores_ph<NBH, QPL, NQB>(ph, kc, smem + w_off + kp * QPL * 8, smem + lw_off + kp * QPL * 4, sc);
+            if constexpr (F8)
+                head_scores_f8<NBH, QPL>(kc, reinterpret_cast<const float*>(smem + w_off) + kp * QPL * 4, sc);
+            else
+                head_scores_ph<NBH, QPL, NQB>(ph, kc, smem + w_off + kp * QPL * 8, smem + lw_off + kp * QPL * 4, sc);
         }
         // ------------------------------------------------ online softmax
         // the lane's queries n = kp * QPL + jj: scale, visible rows, reference max
@@ -771,15 +878,23 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
             const uint32_t sel_lo = vh ? 0x1111u : 0x0000u, sel_hi = vh ? 0x3333u : 0x2222u;
             if (full_tile) {
 #pragma unroll
-                for (int k = 0; k < VR; ++k)
-                    v_row(vb + k * v_step, vh, sel_lo, sel_hi, *reinterpret_cast<const float4*>(pw + k * RG * 4), o2,
-                          pm);
+                for (int k = 0; k < VR; ++k) {
+                    if constexpr (F8)
+                        v_row_f8(vb + k * v_step, *reinterpret_cast<const float4*>(pw + k * RG * 4), o2);
+                    else
+                        v_row(vb + k * v_step, vh, sel_lo, sel_hi, *reinterpret_cast<const float4*>(pw + k * RG * 4),
+                              o2, pm);
+                }
             } else {
 #pragma unroll
                 for (int k = 0; k < VR; ++k)
-                    if (rs * RW + vg + k * RG < nr)
-                        v_row(vb + k * v_step, vh, sel_lo, sel_hi, *reinterpret_cast<const float4*>(pw + k * RG * 4),
-                              o2, pm);
+                    if (rs * RW + vg + k * RG < nr) {
+                        if constexpr (F8)
+                            v_row_f8(vb + k * v_step, *reinterpret_cast<const float4*>(pw + k * RG * 4), o2);
+                        else
+                            v_row(vb + k * v_step, vh, sel_lo, sel_hi,
+                                  *reinterpret_cast<const float4*>(pw + k * RG * 4), o2, pm);
+                    }
             }
         }
         // done with the stage: the last working warp refills it with tile j + NS
@@ -823,15 +938,26 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
                         o2[n][c] = __fadd2_rn(o2[n][c], make_float2(__shfl_xor_sync(0xffffffffu, o2[n][c].x, o),
                                                                     __shfl_xor_sync(0xffffffffu, o2[n][c].y, o)));
                 }
-                // o = sum 256 p d F + sum 256 p (m - 128 d) / 256
-                const float a = pm[n] * (1.f / 256.f);
+                if constexpr (F8) {
+                    // o = sum 256 p v / 256
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    o2[n][c].x += a;
-                    o2[n][c].y += a;
+                    for (int c = 0; c < 8; ++c) {
+                        o2[n][c].x *= 1.f / 256.f;
+                        o2[n][c].y *= 1.f / 256.f;
+                    }
+                } else {
+                    // o = sum 256 p d F + sum 256 p (m - 128 d) / 256
+                    const float a = pm[n] * (1.f / 256.f);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        o2[n][c].x += a;
+                        o2[n][c].y += a;
+                    }
                 }
             }
-            const int dcol = vi * 32 + 8 * vh;          // the lane's dims: dcol + 0..7, dcol + 16..23
+            // the lane's dims: q5_1 dcol + 0..7 and dcol + 16..23; E4M3 dcol + 0..15
+            const int dcol = F8 ? 16 * vhb : vi * 32 + 8 * vh;
+            constexpr int X2 = F8 ? 8 : 16;
             bool write = true;
             if constexpr (RS == 2) {
                 float* so = reinterpret_cast<float*>(smem + L.CB + (size_t)u * (16 * D + 32));   // [4][D], m[4], l[4]
@@ -846,8 +972,8 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
                             float* d4 = so + n * D + dcol;
                             *reinterpret_cast<float4*>(d4) = make_float4(o2[n][0].x, o2[n][0].y, o2[n][1].x, o2[n][1].y);
                             *reinterpret_cast<float4*>(d4 + 4) = make_float4(o2[n][2].x, o2[n][2].y, o2[n][3].x, o2[n][3].y);
-                            *reinterpret_cast<float4*>(d4 + 16) = make_float4(o2[n][4].x, o2[n][4].y, o2[n][5].x, o2[n][5].y);
-                            *reinterpret_cast<float4*>(d4 + 20) = make_float4(o2[n][6].x, o2[n][6].y, o2[n][7].x, o2[n][7].y);
+                            *reinterpret_cast<float4*>(d4 + X2) = make_float4(o2[n][4].x, o2[n][4].y, o2[n][5].x, o2[n][5].y);
+                            *reinterpret_cast<float4*>(d4 + X2 + 4) = make_float4(o2[n][6].x, o2[n][6].y, o2[n][7].x, o2[n][7].y);
                         }
                     }
                     if (lane == 0) {
@@ -873,8 +999,8 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
                             const float* s4 = so + n * D + dcol;
                             const float4 x0 = *reinterpret_cast<const float4*>(s4);
                             const float4 x1 = *reinterpret_cast<const float4*>(s4 + 4);
-                            const float4 x2 = *reinterpret_cast<const float4*>(s4 + 16);
-                            const float4 x3 = *reinterpret_cast<const float4*>(s4 + 20);
+                            const float4 x2 = *reinterpret_cast<const float4*>(s4 + X2);
+                            const float4 x3 = *reinterpret_cast<const float4*>(s4 + X2 + 4);
                             const float xs[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
                                                   x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
@@ -903,8 +1029,8 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
                         float* dst = po + (size_t)off * D;
                         *reinterpret_cast<float4*>(dst) = make_float4(o2[n][0].x, o2[n][0].y, o2[n][1].x, o2[n][1].y);
                         *reinterpret_cast<float4*>(dst + 4) = make_float4(o2[n][2].x, o2[n][2].y, o2[n][3].x, o2[n][3].y);
-                        *reinterpret_cast<float4*>(dst + 16) = make_float4(o2[n][4].x, o2[n][4].y, o2[n][5].x, o2[n][5].y);
-                        *reinterpret_cast<float4*>(dst + 20) = make_float4(o2[n][6].x, o2[n][6].y, o2[n][7].x, o2[n][7].y);
+                        *reinterpret_cast<float4*>(dst + X2) = make_float4(o2[n][4].x, o2[n][4].y, o2[n][5].x, o2[n][5].y);
+                        *reinterpret_cast<float4*>(dst + X2 + 4) = make_float4(o2[n][6].x, o2[n][6].y, o2[n][7].x, o2[n][7].y);
                     }
                     if (lane == 0)
                         *reinterpret_cast<float2*>(pml + (size_t)off * 2) = make_float2(m4[n], l4[n] * (1.f / 256.f));
@@ -1118,10 +1244,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_stream_kernel(const Merge
     }
 }
 
-template <int NBH, int KP, int NQB>
+template <int NBH, int KP, int NQB, bool F8>
 cudaError_t launch_stream_t(const StreamParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, size_t smem,
                             cudaStream_t s) {
-    auto fn = stream_kernel<NBH, KP, NQB>;
+    auto fn = stream_kernel<NBH, KP, NQB, F8>;
     static std::atomic<unsigned long long> attrs{0};
     cudaError_t e = kernel_attrs_once(fn, attrs, true);
     if (e != cudaSuccess) return e;
@@ -1172,9 +1298,14 @@ cudaError_t launch_split_stream(const StreamParams& p, const CUtensorMap& kmap, 
     const int NBH = p.D / 32;
     const int KP = p.RS * 32 / kStreamRows;       // lanes per row in the key phase
 #define KVQ_CASE(nb, kp, nq) \
-    if (NBH == nb && KP == kp && p.qbits == nq) return launch_stream_t<nb, kp, nq>(p, kmap, vmap, smem, s);
+    if (!p.fp8 && NBH == nb && KP == kp && p.qbits == nq) return launch_stream_t<nb, kp, nq, false>(p, kmap, vmap, smem, s);
     KVQ_CASE(2, 1, 16) KVQ_CASE(2, 2, 16) KVQ_CASE(4, 1, 16) KVQ_CASE(4, 2, 16) KVQ_CASE(8, 1, 16) KVQ_CASE(8, 2, 16)
     KVQ_CASE(2, 1, 24) KVQ_CASE(2, 2, 24) KVQ_CASE(4, 1, 24) KVQ_CASE(4, 2, 24) KVQ_CASE(8, 1, 24) KVQ_CASE(8, 2, 24)
+#undef KVQ_CASE
+    // E4M3 rows: the queries stay f32, so the query bits do not apply
+#define KVQ_CASE(nb, kp) \
+    if (p.fp8 && NBH == nb && KP == kp) return launch_stream_t<nb, kp, 16, true>(p, kmap, vmap, smem, s);
+    KVQ_CASE(2, 1) KVQ_CASE(2, 2) KVQ_CASE(4, 1) KVQ_CASE(4, 2) KVQ_CASE(8, 1) KVQ_CASE(8, 2)
 #undef KVQ_CASE
     return cudaErrorInvalidValue;
 }

@@ -132,7 +132,8 @@ struct StreamParams {
     int G;                         // CTAs
     int NS;                        // stages of each of the K and V rings
     uint32_t Sk, Sv;               // shared-memory row strides of the K and V stages
-    int qbits;                     // 16 or 24: query quantisation
+    int qbits;                     // 16 or 24: query quantisation (q8_0 / q5_1 rows)
+    int fp8;                       // 1: both planes hold FP8 E4M3 bytes (kvd per row)
     float* part_o;                 // [slot][4 Hkv QPS][D]: the slice's queries, unit-major
     float* part_ml;                // [slot][4 Hkv QPS][2]  (max in log2 units, sum)
 };
@@ -144,14 +145,16 @@ struct StreamLayout {
 
 __host__ __device__ inline StreamLayout stream_layout(const StreamParams& p) {
     StreamLayout L;
-    const int warps = kStreamThreads / 32;
+    const int warps = p.NA;                         // per-warp areas: the working warps only
     const int RW = kStreamRows / p.RS;
     const int NBH = p.D / 32;
     L.kstage = (uint32_t)kStreamRows * p.Sk;
     L.vstage = (uint32_t)kStreamRows * p.Sv;
     L.pwarp = (uint32_t)RW * 16;                    // [RW rows][4 queries] f32
-    L.wwarp = (uint32_t)NBH * 256;                  // [block][8 pairs of pairs][4 queries][2] 16-bit pairs
-    L.lwarp = p.qbits == 24 ? (uint32_t)NBH * 9 * 16 : 0u;   // [block][9 words][4 queries] low bytes
+    // queries: q8_0 [block][8 pairs of pairs][4 queries][2] 16-bit pairs;
+    // E4M3 [block][8 code words][4 queries][4] f32
+    L.wwarp = p.fp8 ? (uint32_t)NBH * 512 : (uint32_t)NBH * 256;
+    L.lwarp = !p.fp8 && p.qbits == 24 ? (uint32_t)NBH * 9 * 16 : 0u;   // [block][9 words][4 queries] low bytes
     size_t off = 0;
     L.kst = off;
     off += (size_t)p.NS * L.kstage;
@@ -166,7 +169,7 @@ __host__ __device__ inline StreamLayout stream_layout(const StreamParams& p) {
     L.SQ = off;
     off += (size_t)warps * 64;
     L.CB = off;                                     // two row slices: per unit [4][D] sums + 8 floats
-    off += p.RS == 2 ? (size_t)(warps / 2) * (16 * (size_t)p.D + 32) : 0;
+    off += p.RS == 2 ? (size_t)(p.NA / 2) * (16 * (size_t)p.D + 32) : 0;
     L.tabs = off;                                   // len, base, lo, vis, prefix: 5 x (B + 1) ints
     off += fl_round((size_t)5 * (p.B + 1) * 4, 16);
     L.tinfo = off;

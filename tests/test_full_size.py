@@ -60,6 +60,24 @@ def test_ctx32k_full():
     assert c.device_error() == 0
 
 
+def test_ctx32k_full_e4m3():
+    """The 32k workload with FP8 E4M3 K/V planes (stream-K kernel): every
+    row's bytes and every output of the T=1 decode."""
+    wl = workload("ctx32k")
+    L = wl.lengths()[0]
+    c = KVCache(1, wl.n_kv, wl.head_dim, wl.n_q, max_t=64, max_rows=L, fmt="e4m3")
+    k, v = _prefill(c, wl, 0, L)
+    ora = O.OracleKvCache(1, wl.n_kv, wl.head_dim, fmt="e4m3")
+    ora.append(k.numpy()[None], v.numpy()[None])
+    ko, vo = ora.rows(0, 0, L)
+    _rows_equal(c, 0, 0, L, ko, vo, "ctx32k e4m3")
+    q = wl.q(0)
+    got = c.decode(to_dev(q)).cpu().numpy()
+    ref = ora.decode(oracle_input(q))
+    assert_close(got, ref, what="ctx32k e4m3 decode")
+    assert c.device_error() == 0
+
+
 def test_batch64_all_sequences():
     """64 ragged sequences (prefill len-1, one appended row each, T=1
     decode): every sequence byte for byte and output for output."""

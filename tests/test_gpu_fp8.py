@@ -3,10 +3,10 @@ through the C ABI against the fp64 oracle.
 
 Append bytes must be bit-exact, including rounding ties, subnormals, signed
 zeros and saturation beyond 448; attention outputs must be within 2e-3 max abs
-error of the oracle run on the same bytes (the generic split kernel computes
-in fp32, so the error is far below that).  E4M3 caches decode on the generic
-kernel: automatic choice picks it, and forcing the warp-specialised kernel is
-refused."""
+error of the oracle run on the same bytes (both kernels decode E4M3 exactly
+and compute in fp32, so the error is far below that).  E4M3 caches decode on
+the stream-K kernel where its geometry allows (head_dim 64, 128 or 256, token
+rows of 16-byte multiples), else on the generic split kernel."""
 
 import numpy as np
 import pytest
@@ -91,12 +91,18 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("path", [0, 1], ids=["auto", "generic"])
+@pytest.mark.parametrize("path", [0, 1, 2], ids=["auto", "generic", "stream"])
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
 def test_fp8_decode_matches_oracle(case, path):
     Bn, Hq, Hkv, D, lens, T, window, ring, sinks, qdt = case
     p = Pair(Bn, Hkv, D, Hq, max_t=max(T, 64), max_rows=max(lens) + T, window=window, ring=ring, fmt=F8)
     p.dev.set_decode_path(path)
+    if path == 2 and (D not in (64, 128, 256) or (Hkv * D) % 16):
+        p.append(_randn(Bn, 1, Hkv, D, seed=1), _randn(Bn, 1, Hkv, D, seed=2))
+        with pytest.raises(B.KvqError) as e:
+            p.dev.decode(to_dev(_randn(Bn, 1, Hq, D, seed=3)))
+        assert e.value.status == B.KVQ_EUNSUPPORTED
+        return
     for b, L in enumerate(lens):
         k = _randn(1, L, Hkv, D, seed=100 + b, scale=2.0)
         v = _randn(1, L, Hkv, D, seed=200 + b)
@@ -110,13 +116,25 @@ def test_fp8_decode_matches_oracle(case, path):
     assert p.dev.device_error() == 0
 
 
-def test_fp8_warp_specialised_path_refused():
-    p = Pair(1, 8, 128, 32, max_t=64, max_rows=256, fmt=F8)
-    k = _randn(1, 200, 8, 128, seed=5)
-    p.append(k[:, :64], k[:, :64])
+def test_fp8_stream_kernel_equals_generic_and_refuses_head_dim_32():
+    """Forced onto the stream-K kernel an E4M3 cache gives the generic
+    kernel's result to fp32 rounding; a head_dim it does not take is refused."""
+    p = Pair(2, 8, 128, 32, max_t=64, max_rows=700, fmt=F8)
+    for b, L in enumerate((640, 333)):
+        k = _randn(1, L, 8, 128, seed=5 + b, scale=3.0)
+        for t0 in range(0, L, 64):
+            p.append(k[:, t0:t0 + 64], -k[:, t0:t0 + 64], seq_ids=[b])
+    q = to_dev(_randn(2, 1, 32, 128, seed=6))
     p.dev.set_decode_path(2)
+    stream = p.dev.decode(q).cpu().numpy()
+    p.dev.set_decode_path(1)
+    generic = p.dev.decode(q).cpu().numpy()
+    assert np.max(np.abs(stream - generic)) <= 1e-5
+    small = Pair(1, 4, 32, 8, max_t=8, max_rows=64, fmt=F8)
+    small.append(_randn(1, 8, 4, 32, seed=7), _randn(1, 8, 4, 32, seed=8))
+    small.dev.set_decode_path(2)
     with pytest.raises(B.KvqError) as e:
-        p.dev.decode(to_dev(_randn(1, 1, 32, 128, seed=6)))
+        small.dev.decode(to_dev(_randn(1, 1, 8, 32, seed=9)))
     assert e.value.status == B.KVQ_EUNSUPPORTED
     assert p.dev.device_error() == 0
 
@@ -129,6 +147,7 @@ def test_fp8_split_sizes_agree(split_rows):
         k = _randn(1, L - 100 * b, Hkv, D, seed=300 + b)
         for t0 in range(0, k.shape[1], 64):
             p.append(k[:, t0:t0 + 64], 0.5 * k[:, t0:t0 + 64], seq_ids=[b])
+    p.dev.set_decode_path(1)                    # split sizes belong to the generic kernel
     p.dev.set_split_rows(split_rows)
     got, ref = p.decode(_randn(2, 1, Hq, D, seed=9))
     assert_close(got, ref)
