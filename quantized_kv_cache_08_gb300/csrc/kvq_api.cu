@@ -431,7 +431,6 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         p.NA = Hkv * sh.QPS * sh.RS;
         p.Qtot = n_q_heads * T;
         p.qbits = c->qbits;
-        p.fp8 = c->fp8 ? 1 : 0;
         p.Sk = c->Sk;
         p.Sv = c->Sv;
         // CTAs: one per SM, fewer when there are fewer 32-row tiles of work
@@ -448,8 +447,9 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         }
         const int smem_max = stream_max_smem();
         p.NS = 3;
-        while (p.NS > 2 && stream_layout(p).total > (size_t)smem_max) --p.NS;
-        if (stream_layout(p).total <= (size_t)smem_max) {
+        auto layout_bytes = [&]() { return c->fp8 ? stream_layout_f8(p).total : stream_layout(p).total; };
+        while (p.NS > 2 && layout_bytes() > (size_t)smem_max) --p.NS;
+        if (layout_bytes() <= (size_t)smem_max) {
             const size_t recs = stream_records(&c->cfg, sh, p.G);
             if (scratch) {
                 const size_t o_ml = round_up(recs * D * sizeof(float), 256);
@@ -464,7 +464,8 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
                 p.part_o = reinterpret_cast<float*>(c->ws + c->off_part_o);
                 p.part_ml = reinterpret_cast<float*>(c->ws + c->off_part_ml);
             }
-            cudaError_t e = launch_split_stream(p, c->kmap, c->vmap, s);
+            cudaError_t e = c->fp8 ? launch_split_stream_f8(p, c->kmap, c->vmap, s)
+                                   : launch_split_stream(p, c->kmap, c->vmap, s);
             if (e != cudaSuccess) return cuda_fail(e, "decode split kernel");
             MergeStreamParams m;
             m.part_o = p.part_o;

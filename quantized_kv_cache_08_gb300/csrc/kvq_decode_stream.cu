@@ -41,15 +41,27 @@
 // of its half block with byte arithmetic, places each in the mantissa of 0.5
 // (value 0.5 + u/256), so v_hat = 256 d F + (m - 128 d), and accumulates
 // o += (256 p d) F with packed FMAs and sum p (m - 128 d) per block.
-// E4M3 rows (template flag F8): the queries stay f32; each code word of K
-// and V becomes four exact floats (an E4M3 pair converts to a half pair, then
-// to floats) and both phases multiply with packed FMAs; a V lane takes 16
-// contiguous dims.
+// E4M3 rows: this file compiled with KVQ_STREAM_F8 (kvq_decode_stream_f8.cu)
+// gives stream_kernel_f8, whose queries stay f32; each code word of K and V
+// becomes four exact floats (an E4M3 pair converts to a half pair, then to
+// floats) and both phases multiply with packed FMAs; a V lane takes 16
+// contiguous dims.  Everything else is shared line for line, and the q8_0 /
+// q5_1 build of the file sees none of the E4M3 code.
+#define KVQ_STREAM_TU 1
 #include "kvq_device.cuh"
 
-#include <cuda_fp8.h>
-
 #include <type_traits>
+
+#if KVQ_STREAM_F8
+#include <cuda_fp8.h>
+#define KVQ_STREAM_KERNEL stream_kernel_f8
+#define KVQ_LAYOUT stream_layout_f8
+#define KVQ_X2 8
+#else
+#define KVQ_STREAM_KERNEL stream_kernel
+#define KVQ_LAYOUT stream_layout
+#define KVQ_X2 16
+#endif
 
 namespace kvq {
 namespace {
@@ -481,6 +493,7 @@ __device__ __forceinline__ void v_row(const uint8_t* vb, int h, uint32_t sel_lo,
     }
 }
 
+#if KVQ_STREAM_F8
 // ------------------------------------------------------------ FP8 E4M3 rows
 
 // Two E4M3 bytes (element order: low byte first) as two floats, exactly.
@@ -573,10 +586,12 @@ __device__ __forceinline__ void v_row_f8(const uint8_t* vb, const float4 p4, flo
     }
 }
 
+#endif  // KVQ_STREAM_F8
+
 // ------------------------------------------------------------ the kernel
 
-template <int NBH, int KP, int NQB, bool F8>
-__global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(const StreamParams p,
+template <int NBH, int KP, int NQB>
+__global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) KVQ_STREAM_KERNEL(const StreamParams p,
                                                               const __grid_constant__ CUtensorMap kmap,
                                                               const __grid_constant__ CUtensorMap vmap) {
     constexpr int D = NBH * 32;
@@ -591,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
     extern __shared__ __align__(128) uint8_t smem_raw[];
     // TMA tile destinations need 128-byte alignment
     uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-    const StreamLayout L = stream_layout(p);
+    const StreamLayout L = KVQ_LAYOUT(p);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.B, NS = p.NS;
     int* s_tab = reinterpret_cast<int*>(smem + L.tabs);
@@ -711,16 +726,22 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
     // K-phase lane: row kr of the warp's slice, part kp (queries kp*QPL..)
     const int kr = lane / KP, kp = lane - kr * KP;
     const int trow = rs * RW + kr;                  // tile row of this K lane
-    // byte of the head's first K block in a row (q8_0: 34 B blocks; E4M3: D B)
-    const int hb0 = F8 ? D * g : 34 * NBH * g;
+#if KVQ_STREAM_F8
+    const int hb0 = D * g;                          // byte of the head's row in a token row
+#else
+    const int hb0 = 34 * NBH * g;                   // byte of the head's first K block in a row
+#endif
     const int ph = hb0 & 15;
     const uint32_t k_lane_off = (uint32_t)L.kst + (uint32_t)trow * p.Sk + (uint32_t)(hb0 - ph);
     // V-phase lane: row group vg, half block vh of block vi
     const int vg = lane / VH, vhb = lane - vg * VH;
     const int vi = vhb >> 1, vh = vhb & 1;
-    // q5_1: half block vh of block vi (24 B blocks); E4M3: 16 contiguous dims
-    const uint32_t v_lane_off = (uint32_t)L.vst + (uint32_t)(rs * RW + vg) * p.Sv +
-                                (uint32_t)(F8 ? D * g + 16 * vhb : 24 * (NBH * g + vi));
+#if KVQ_STREAM_F8
+    // 16 contiguous dims of the head
+    const uint32_t v_lane_off = (uint32_t)L.vst + (uint32_t)(rs * RW + vg) * p.Sv + (uint32_t)(D * g + 16 * vhb);
+#else
+    const uint32_t v_lane_off = (uint32_t)L.vst + (uint32_t)(rs * RW + vg) * p.Sv + (uint32_t)(24 * (NBH * g + vi));
+#endif
     const uint32_t v_step = (uint32_t)RG * p.Sv;
 
     float lsum[QPL], sq[QPL], pm[4];
@@ -743,11 +764,12 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
     auto begin_fragment = [&](int b, int qs) {
         key = b * 65536 + qs;
         const int qg = qs * p.QPS + qgl;
-        if constexpr (F8)
-            prep_queries_f8<NBH>(p, b, g, qg, reinterpret_cast<float*>(smem + w_off), STw + 4, lane);
-        else
+#if KVQ_STREAM_F8
+        prep_queries_f8<NBH>(p, b, g, qg, reinterpret_cast<float*>(smem + w_off), STw + 4, lane);
+#else
         prep_queries<NBH, NQB>(p, b, g, qg, reinterpret_cast<uint32_t*>(smem + w_off), smem + lw_off, STw + 4,
                                lane);
+#endif
         if (lane < 4) {
             const int qi = 4 * qg + lane;
             int lo = 0, hi = -1;
@@ -795,10 +817,11 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
         for (int jj = 0; jj < QPL; ++jj) sc[jj] = 0.f;
         if (full_tile || trow < nr) {
             const uint4* kc = reinterpret_cast<const uint4*>(smem + k_lane_off + (uint32_t)st * L.kstage);
-            if constexpr (F8)
-                head_scores_f8<NBH, QPL>(kc, reinterpret_cast<const float*>(smem + w_off) + kp * QPL * 4, sc);
-            else
-                head_scores_ph<NBH, QPL, NQB>(ph, kc, smem + w_off + kp * QPL * 8, smem + lw_off + kp * QPL * 4, sc);
+#if KVQ_STREAM_F8
+            head_scores_f8<NBH, QPL>(kc, reinterpret_cast<const float*>(smem + w_off) + kp * QPL * 4, sc);
+#else
+            head_scores_ph<NBH, QPL, NQB>(ph, kc, smem + w_off + kp * QPL * 8, smem + lw_off + kp * QPL * 4, sc);
+#endif
         }
         // ------------------------------------------------ online softmax
         // the lane's queries n = kp * QPL + jj: scale, visible rows, reference max
@@ -876,26 +899,31 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
             const uint8_t* vb = smem + v_lane_off + (uint32_t)st * L.vstage;
             const float* pw = reinterpret_cast<const float*>(smem + p_off) + vg * 4;
             const uint32_t sel_lo = vh ? 0x1111u : 0x0000u, sel_hi = vh ? 0x3333u : 0x2222u;
+#if KVQ_STREAM_F8
             if (full_tile) {
 #pragma unroll
-                for (int k = 0; k < VR; ++k) {
-                    if constexpr (F8)
-                        v_row_f8(vb + k * v_step, *reinterpret_cast<const float4*>(pw + k * RG * 4), o2);
-                    else
-                        v_row(vb + k * v_step, vh, sel_lo, sel_hi, *reinterpret_cast<const float4*>(pw + k * RG * 4),
-                              o2, pm);
-                }
+                for (int k = 0; k < VR; ++k)
+                    v_row_f8(vb + k * v_step, *reinterpret_cast<const float4*>(pw + k * RG * 4), o2);
             } else {
 #pragma unroll
                 for (int k = 0; k < VR; ++k)
-                    if (rs * RW + vg + k * RG < nr) {
-                        if constexpr (F8)
-                            v_row_f8(vb + k * v_step, *reinterpret_cast<const float4*>(pw + k * RG * 4), o2);
-                        else
-                            v_row(vb + k * v_step, vh, sel_lo, sel_hi,
-                                  *reinterpret_cast<const float4*>(pw + k * RG * 4), o2, pm);
-                    }
+                    if (rs * RW + vg + k * RG < nr)
+                        v_row_f8(vb + k * v_step, *reinterpret_cast<const float4*>(pw + k * RG * 4), o2);
             }
+#else
+            if (full_tile) {
+#pragma unroll
+                for (int k = 0; k < VR; ++k)
+                    v_row(vb + k * v_step, vh, sel_lo, sel_hi, *reinterpret_cast<const float4*>(pw + k * RG * 4), o2,
+                          pm);
+            } else {
+#pragma unroll
+                for (int k = 0; k < VR; ++k)
+                    if (rs * RW + vg + k * RG < nr)
+                        v_row(vb + k * v_step, vh, sel_lo, sel_hi, *reinterpret_cast<const float4*>(pw + k * RG * 4),
+                              o2, pm);
+            }
+#endif
         }
         // done with the stage: the last working warp refills it with tile j + NS
         __syncwarp();
@@ -938,26 +966,28 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
                         o2[n][c] = __fadd2_rn(o2[n][c], make_float2(__shfl_xor_sync(0xffffffffu, o2[n][c].x, o),
                                                                     __shfl_xor_sync(0xffffffffu, o2[n][c].y, o)));
                 }
-                if constexpr (F8) {
-                    // o = sum 256 p v / 256
+#if KVQ_STREAM_F8
+                // o = sum 256 p v / 256
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        o2[n][c].x *= 1.f / 256.f;
-                        o2[n][c].y *= 1.f / 256.f;
-                    }
-                } else {
-                    // o = sum 256 p d F + sum 256 p (m - 128 d) / 256
-                    const float a = pm[n] * (1.f / 256.f);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        o2[n][c].x += a;
-                        o2[n][c].y += a;
-                    }
+                for (int c = 0; c < 8; ++c) {
+                    o2[n][c].x *= 1.f / 256.f;
+                    o2[n][c].y *= 1.f / 256.f;
                 }
+#else
+                // o = sum 256 p d F + sum 256 p (m - 128 d) / 256
+                const float a = pm[n] * (1.f / 256.f);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    o2[n][c].x += a;
+                    o2[n][c].y += a;
+                }
+#endif
             }
-            // the lane's dims: q5_1 dcol + 0..7 and dcol + 16..23; E4M3 dcol + 0..15
-            const int dcol = F8 ? 16 * vhb : vi * 32 + 8 * vh;
-            constexpr int X2 = F8 ? 8 : 16;
+#if KVQ_STREAM_F8
+            const int dcol = 16 * vhb;                  // the lane's dims: dcol + 0..15
+#else
+            const int dcol = vi * 32 + 8 * vh;          // the lane's dims: dcol + 0..7, dcol + 16..23
+#endif
             bool write = true;
             if constexpr (RS == 2) {
                 float* so = reinterpret_cast<float*>(smem + L.CB + (size_t)u * (16 * D + 32));   // [4][D], m[4], l[4]
@@ -972,8 +1002,8 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
                             float* d4 = so + n * D + dcol;
                             *reinterpret_cast<float4*>(d4) = make_float4(o2[n][0].x, o2[n][0].y, o2[n][1].x, o2[n][1].y);
                             *reinterpret_cast<float4*>(d4 + 4) = make_float4(o2[n][2].x, o2[n][2].y, o2[n][3].x, o2[n][3].y);
-                            *reinterpret_cast<float4*>(d4 + X2) = make_float4(o2[n][4].x, o2[n][4].y, o2[n][5].x, o2[n][5].y);
-                            *reinterpret_cast<float4*>(d4 + X2 + 4) = make_float4(o2[n][6].x, o2[n][6].y, o2[n][7].x, o2[n][7].y);
+                            *reinterpret_cast<float4*>(d4 + KVQ_X2) = make_float4(o2[n][4].x, o2[n][4].y, o2[n][5].x, o2[n][5].y);
+                            *reinterpret_cast<float4*>(d4 + KVQ_X2 + 4) = make_float4(o2[n][6].x, o2[n][6].y, o2[n][7].x, o2[n][7].y);
                         }
                     }
                     if (lane == 0) {
@@ -999,8 +1029,8 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
                             const float* s4 = so + n * D + dcol;
                             const float4 x0 = *reinterpret_cast<const float4*>(s4);
                             const float4 x1 = *reinterpret_cast<const float4*>(s4 + 4);
-                            const float4 x2 = *reinterpret_cast<const float4*>(s4 + X2);
-                            const float4 x3 = *reinterpret_cast<const float4*>(s4 + X2 + 4);
+                            const float4 x2 = *reinterpret_cast<const float4*>(s4 + KVQ_X2);
+                            const float4 x3 = *reinterpret_cast<const float4*>(s4 + KVQ_X2 + 4);
                             const float xs[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
                                                   x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
@@ -1029,8 +1059,8 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
                         float* dst = po + (size_t)off * D;
                         *reinterpret_cast<float4*>(dst) = make_float4(o2[n][0].x, o2[n][0].y, o2[n][1].x, o2[n][1].y);
                         *reinterpret_cast<float4*>(dst + 4) = make_float4(o2[n][2].x, o2[n][2].y, o2[n][3].x, o2[n][3].y);
-                        *reinterpret_cast<float4*>(dst + X2) = make_float4(o2[n][4].x, o2[n][4].y, o2[n][5].x, o2[n][5].y);
-                        *reinterpret_cast<float4*>(dst + X2 + 4) = make_float4(o2[n][6].x, o2[n][6].y, o2[n][7].x, o2[n][7].y);
+                        *reinterpret_cast<float4*>(dst + KVQ_X2) = make_float4(o2[n][4].x, o2[n][4].y, o2[n][5].x, o2[n][5].y);
+                        *reinterpret_cast<float4*>(dst + KVQ_X2 + 4) = make_float4(o2[n][6].x, o2[n][6].y, o2[n][7].x, o2[n][7].y);
                     }
                     if (lane == 0)
                         *reinterpret_cast<float2*>(pml + (size_t)off * 2) = make_float2(m4[n], l4[n] * (1.f / 256.f));
@@ -1059,6 +1089,7 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
     }
 }
 
+#if !KVQ_STREAM_F8
 // ------------------------------------------------------------- the merge
 
 // Combine the partial records of one (sequence, query) over the fragments of
@@ -1244,10 +1275,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_stream_kernel(const Merge
     }
 }
 
-template <int NBH, int KP, int NQB, bool F8>
+#endif  // !KVQ_STREAM_F8
+
+template <int NBH, int KP, int NQB>
 cudaError_t launch_stream_t(const StreamParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, size_t smem,
                             cudaStream_t s) {
-    auto fn = stream_kernel<NBH, KP, NQB, F8>;
+    auto fn = KVQ_STREAM_KERNEL<NBH, KP, NQB>;
     static std::atomic<unsigned long long> attrs{0};
     cudaError_t e = kernel_attrs_once(fn, attrs, true);
     if (e != cudaSuccess) return e;
@@ -1266,6 +1299,7 @@ cudaError_t launch_stream_t(const StreamParams& p, const CUtensorMap& kmap, cons
     return cudaGetLastError();
 }
 
+#if !KVQ_STREAM_F8
 template <int VPL, int U>
 cudaError_t launch_merge_stream_t(const MergeStreamParams& p, cudaStream_t s) {
     const int PPC = kMergeWarps / p.WPQ;
@@ -1290,22 +1324,20 @@ cudaError_t launch_merge_stream_t(const MergeStreamParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+#endif  // !KVQ_STREAM_F8
+
 }  // namespace
 
+#if !KVQ_STREAM_F8
 cudaError_t launch_split_stream(const StreamParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                 cudaStream_t s) {
     const size_t smem = stream_layout(p).total;
     const int NBH = p.D / 32;
     const int KP = p.RS * 32 / kStreamRows;       // lanes per row in the key phase
 #define KVQ_CASE(nb, kp, nq) \
-    if (!p.fp8 && NBH == nb && KP == kp && p.qbits == nq) return launch_stream_t<nb, kp, nq, false>(p, kmap, vmap, smem, s);
+    if (NBH == nb && KP == kp && p.qbits == nq) return launch_stream_t<nb, kp, nq>(p, kmap, vmap, smem, s);
     KVQ_CASE(2, 1, 16) KVQ_CASE(2, 2, 16) KVQ_CASE(4, 1, 16) KVQ_CASE(4, 2, 16) KVQ_CASE(8, 1, 16) KVQ_CASE(8, 2, 16)
     KVQ_CASE(2, 1, 24) KVQ_CASE(2, 2, 24) KVQ_CASE(4, 1, 24) KVQ_CASE(4, 2, 24) KVQ_CASE(8, 1, 24) KVQ_CASE(8, 2, 24)
-#undef KVQ_CASE
-    // E4M3 rows: the queries stay f32, so the query bits do not apply
-#define KVQ_CASE(nb, kp) \
-    if (p.fp8 && NBH == nb && KP == kp) return launch_stream_t<nb, kp, 16, true>(p, kmap, vmap, smem, s);
-    KVQ_CASE(2, 1) KVQ_CASE(2, 2) KVQ_CASE(4, 1) KVQ_CASE(4, 2) KVQ_CASE(8, 1) KVQ_CASE(8, 2)
 #undef KVQ_CASE
     return cudaErrorInvalidValue;
 }
@@ -1353,5 +1385,19 @@ int stream_max_smem() {
     cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     return v - 256;  // static shared variables
 }
+
+#else
+cudaError_t launch_split_stream_f8(const StreamParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                   cudaStream_t s) {
+    const size_t smem = stream_layout_f8(p).total;
+    const int NBH = p.D / 32;
+    const int KP = p.RS * 32 / kStreamRows;       // lanes per row in the key phase
+#define KVQ_CASE(nb, kp) \
+    if (NBH == nb && KP == kp) return launch_stream_t<nb, kp, 16>(p, kmap, vmap, smem, s);
+    KVQ_CASE(2, 1) KVQ_CASE(2, 2) KVQ_CASE(4, 1) KVQ_CASE(4, 2) KVQ_CASE(8, 1) KVQ_CASE(8, 2)
+#undef KVQ_CASE
+    return cudaErrorInvalidValue;
+}
+#endif  // !KVQ_STREAM_F8
 
 }  // namespace kvq

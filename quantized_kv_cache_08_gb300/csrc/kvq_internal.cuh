@@ -132,8 +132,7 @@ struct StreamParams {
     int G;                         // CTAs
     int NS;                        // stages of each of the K and V rings
     uint32_t Sk, Sv;               // shared-memory row strides of the K and V stages
-    int qbits;                     // 16 or 24: query quantisation (q8_0 / q5_1 rows)
-    int fp8;                       // 1: both planes hold FP8 E4M3 bytes (kvd per row)
+    int qbits;                     // 16 or 24: query quantisation
     float* part_o;                 // [slot][4 Hkv QPS][D]: the slice's queries, unit-major
     float* part_ml;                // [slot][4 Hkv QPS][2]  (max in log2 units, sum)
 };
@@ -145,16 +144,57 @@ struct StreamLayout {
 
 __host__ __device__ inline StreamLayout stream_layout(const StreamParams& p) {
     StreamLayout L;
-    const int warps = p.NA;                         // per-warp areas: the working warps only
+    const int warps = kStreamThreads / 32;
     const int RW = kStreamRows / p.RS;
     const int NBH = p.D / 32;
     L.kstage = (uint32_t)kStreamRows * p.Sk;
     L.vstage = (uint32_t)kStreamRows * p.Sv;
     L.pwarp = (uint32_t)RW * 16;                    // [RW rows][4 queries] f32
-    // queries: q8_0 [block][8 pairs of pairs][4 queries][2] 16-bit pairs;
-    // E4M3 [block][8 code words][4 queries][4] f32
-    L.wwarp = p.fp8 ? (uint32_t)NBH * 512 : (uint32_t)NBH * 256;
-    L.lwarp = !p.fp8 && p.qbits == 24 ? (uint32_t)NBH * 9 * 16 : 0u;   // [block][9 words][4 queries] low bytes
+    L.wwarp = (uint32_t)NBH * 256;                  // [block][8 pairs of pairs][4 queries][2] 16-bit pairs
+    L.lwarp = p.qbits == 24 ? (uint32_t)NBH * 9 * 16 : 0u;   // [block][9 words][4 queries] low bytes
+    size_t off = 0;
+    L.kst = off;
+    off += (size_t)p.NS * L.kstage;
+    L.vst = off;
+    off += (size_t)p.NS * L.vstage;
+    L.P = off;
+    off += (size_t)warps * L.pwarp;
+    L.W = off;
+    off += (size_t)warps * L.wwarp;
+    L.LW = off;
+    off += (size_t)warps * L.lwarp;
+    L.SQ = off;
+    off += (size_t)warps * 64;
+    L.CB = off;                                     // two row slices: per unit [4][D] sums + 8 floats
+    off += p.RS == 2 ? (size_t)(warps / 2) * (16 * (size_t)p.D + 32) : 0;
+    L.tabs = off;                                   // len, base, lo, vis, prefix: 5 x (B + 1) ints
+    off += fl_round((size_t)5 * (p.B + 1) * 4, 16);
+    L.tinfo = off;
+    off += (size_t)2 * p.NS * 16;
+    L.bars = off;
+    off += (size_t)2 * p.NS * 8;
+    L.cnt = off;                                    // release counters and armed-phase counts
+    off += fl_round((size_t)4 * p.NS * 4, 16);
+    L.walk = off;
+    off += 64;
+    L.total = off + 128;                            // slack to align the base to 128 bytes
+    return L;
+}
+
+// The layout of the E4M3 kernel: per-warp areas for the working warps only
+// (1 KB token rows leave no room for idle warps' areas with three stages),
+// f32 query words.  Left out of the q8_0 / q5_1 kernel's translation unit.
+#if !defined(KVQ_STREAM_TU) || defined(KVQ_STREAM_F8)
+__host__ __device__ inline StreamLayout stream_layout_f8(const StreamParams& p) {
+    StreamLayout L;
+    const int warps = p.NA;
+    const int RW = kStreamRows / p.RS;
+    const int NBH = p.D / 32;
+    L.kstage = (uint32_t)kStreamRows * p.Sk;
+    L.vstage = (uint32_t)kStreamRows * p.Sv;
+    L.pwarp = (uint32_t)RW * 16;                    // [RW rows][4 queries] f32
+    L.wwarp = (uint32_t)NBH * 512;                  // [block][8 code words][4 queries][4] f32
+    L.lwarp = 0u;
     size_t off = 0;
     L.kst = off;
     off += (size_t)p.NS * L.kstage;
@@ -183,6 +223,7 @@ __host__ __device__ inline StreamLayout stream_layout(const StreamParams& p) {
     L.total = off + 128;                            // slack to align the base to 128 bytes
     return L;
 }
+#endif
 
 struct MergeStreamParams {
     const float* part_o;
@@ -231,6 +272,9 @@ cudaError_t launch_split(const SplitParams& p, int grid, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, int T, int max_splits, bool pdl, cudaStream_t s);
 
 // stream-K decode (kvq_decode_stream.cu): token rows must be 16-byte multiples
+// the stream-K split kernel for FP8 E4M3 rows (its own translation unit)
+cudaError_t launch_split_stream_f8(const StreamParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                   cudaStream_t s);
 cudaError_t launch_split_stream(const StreamParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                 cudaStream_t s);
 // 2-D TMA map of a byte plane of `rows` token rows of tok_bytes (a multiple of
