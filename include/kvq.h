@@ -291,6 +291,14 @@ kvq_status kvq_set_decode_path(kvq_cache* cache, int path, int query_bits);
  * non-finite value. */
 kvq_status kvq_set_softcap(kvq_cache* cache, float softcap);
 
+/* Row slices per 32-row tile on the stream-K kernel: 0 = automatic (two,
+ * one warp per half tile, when 2 x (KV heads x four-query groups of a slice)
+ * <= 16 and the CTAs have more than 16 tiles each; else one), 1, or 2 (taken
+ * only where the geometry allows two; else one).  Results are the same up to
+ * fp32 rounding; the choice moves speed only.  No passage: a tuning knob of
+ * this implementation.  KVQ_EINVAL for another value. */
+kvq_status kvq_set_row_slices(kvq_cache* cache, int slices);
+
 /* Override the generic kernel's split size in rows (a multiple of 8, >= 64;
  * 0 = auto).  The stream-K kernel ignores it: its CTAs split the rows
  * evenly. */

@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ERANGE", 3: "KVQ_ECUDA", 4
 EXPORTS = (
     "kvq_required_bytes", "kvq_alloc", "kvq_free", "kvq_append", "kvq_decode",
     "kvq_decode_noalloc", "kvq_truncate", "kvq_truncate_device", "kvq_sync_len", "kvq_get_len", "kvq_note_replayed", "kvq_ring_headroom",
-    "kvq_physical_rows", "kvq_read_device_error", "kvq_set_split_rows", "kvq_set_decode_path",
+    "kvq_physical_rows", "kvq_read_device_error", "kvq_set_split_rows", "kvq_set_row_slices", "kvq_set_decode_path",
     "kvq_set_softcap",
     "kvq_block_bytes", "kvq_bytes_per_token", "kvq_last_error",
 )
@@ -82,6 +82,7 @@ def lib():
             "kvq_physical_rows": (I, [P, I, I, I, IP, IP]),
             "kvq_read_device_error": (I, [P, IP, P]),
             "kvq_set_split_rows": (I, [P, I]),
+            "kvq_set_row_slices": (I, [P, I]),
             "kvq_set_decode_path": (I, [P, I, I]),
             "kvq_set_softcap": (I, [P, ctypes.c_float]),
             "kvq_block_bytes": (I, [I]),
@@ -188,6 +189,10 @@ def kvq_read_device_error(handle, stream=0):
 
 def kvq_set_split_rows(handle, rows):
     _check(lib().kvq_set_split_rows(handle, rows))
+
+
+def kvq_set_row_slices(handle, slices):
+    _check(lib().kvq_set_row_slices(handle, slices))
 
 
 def kvq_set_decode_path(handle, path, query_bits=0):

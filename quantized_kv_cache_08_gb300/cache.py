@@ -137,12 +137,16 @@ class KVCache:
     def set_split_rows(self, rows):
         B.kvq_set_split_rows(self.handle, rows)
 
+    def set_row_slices(self, slices):
+        """Row slices per tile on the stream-K kernel: 0 automatic, 1 or 2."""
+        B.kvq_set_row_slices(self.handle, slices)
+
     def set_softcap(self, softcap):
         """softcap > 0 caps scaled scores to softcap * tanh(s / softcap); 0 is off."""
         B.kvq_set_softcap(self.handle, softcap)
 
     def set_decode_path(self, path, query_bits=0):
-        """path: 0 auto, 1 generic split kernel, 2 warp-specialised kernel."""
+        """path: 0 auto, 1 generic split kernel, 2 stream-K kernel."""
         B.kvq_set_decode_path(self.handle, path, query_bits)
 
     def k_rows(self, seq, phys_lo, phys_hi):

@@ -32,6 +32,7 @@ struct kvq_cache {
     int max_vis;                         // most rows one decode may read per sequence
     int num_sms;
     int split_rows;                      // 0 = automatic
+    int row_slices;                      // stream-K row slices per tile: 0 = automatic, 1 or 2
     int path;                            // 0 auto, 1 generic split kernel, 2 stream-K kernel
     int qbits;                           // query bits of the stream-K kernel (16 or 24)
     int fp8;                             // 1: K and V planes hold FP8 E4M3 bytes
@@ -235,6 +236,7 @@ kvq_status kvq_alloc(const kvq_config* cfg, void* k_plane, void* v_plane, void* 
     c->max_vis = g.max_vis;
     c->num_sms = sms;
     c->split_rows = 0;
+    c->row_slices = 0;
     // stream-K stage rows: K at an odd multiple of 16 bytes (consecutive rows
     // in different bank groups), V at 64 mod 128 bytes
     // (rows that are not 16-byte multiples cannot be tensor-copied at all)
@@ -441,7 +443,8 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, kvq_dtype dtype, int 
         // hide more latency); with few tiles per CTA one slice wins (half the
         // query preparation, no pair hand-over at a record): measured on
         // GB300 the turn is near 16 tiles per CTA
-        if (p.RS == 2 && work <= kStreamShortTiles * kStreamRows * (long long)p.G) {
+        if (p.RS == 2 && (c->row_slices == 1 ||
+                          (c->row_slices == 0 && work <= kStreamShortTiles * kStreamRows * (long long)p.G))) {
             p.RS = 1;
             p.NA = Hkv * sh.QPS;
         }
@@ -787,6 +790,13 @@ kvq_status kvq_set_decode_path(kvq_cache* c, int path, int query_bits) {
         return fail(KVQ_EINVAL, "query_bits must be 0, 16 or 24");
     c->path = path;
     c->qbits = query_bits == 24 ? 24 : 16;
+    return KVQ_OK;
+}
+
+kvq_status kvq_set_row_slices(kvq_cache* c, int slices) {
+    if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+    if (slices < 0 || slices > 2) return fail(KVQ_EINVAL, "row slices must be 0, 1 or 2");
+    c->row_slices = slices;
     return KVQ_OK;
 }
 

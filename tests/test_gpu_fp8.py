@@ -91,13 +91,14 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("path", [0, 1, 2], ids=["auto", "generic", "stream"])
+@pytest.mark.parametrize("path", [0, 1, 2, 3], ids=["auto", "generic", "stream", "stream_rs2"])
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
 def test_fp8_decode_matches_oracle(case, path):
     Bn, Hq, Hkv, D, lens, T, window, ring, sinks, qdt = case
     p = Pair(Bn, Hkv, D, Hq, max_t=max(T, 64), max_rows=max(lens) + T, window=window, ring=ring, fmt=F8)
-    p.dev.set_decode_path(path)
-    if path == 2 and (D not in (64, 128, 256) or (Hkv * D) % 16):
+    p.dev.set_decode_path(min(path, 2))
+    p.dev.set_row_slices(2 if path == 3 else 0)
+    if path >= 2 and (D not in (64, 128, 256) or (Hkv * D) % 16):
         p.append(_randn(Bn, 1, Hkv, D, seed=1), _randn(Bn, 1, Hkv, D, seed=2))
         with pytest.raises(B.KvqError) as e:
             p.dev.decode(to_dev(_randn(Bn, 1, Hq, D, seed=3)))

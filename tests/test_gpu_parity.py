@@ -128,15 +128,19 @@ CASES = [
 ]
 
 # (kernel path, query bits): 1 = generic split kernel, 2 = stream-K kernel
-PATHS = [(1, 0), (2, 24), (2, 16)]
+# (kernel path, query bits, row slices): the generic kernel, the stream-K
+# kernel with 24- and 16-bit queries, and the stream-K kernel with two row
+# slices forced (small shapes otherwise take one: few tiles per CTA)
+PATHS = [(1, 0, 0), (2, 24, 0), (2, 16, 0), (2, 16, 2)]
 
 
-@pytest.mark.parametrize("path", PATHS, ids=["generic", "ws24", "ws16"])
+@pytest.mark.parametrize("path", PATHS, ids=["generic", "ws24", "ws16", "ws16rs2"])
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
 def test_decode_matches_oracle(case, path):
     Bn, Hq, Hkv, D, lens, T, window, ring, sinks, qdt = case
     p = Pair(Bn, Hkv, D, Hq, max_t=max(T, 64), max_rows=max(lens) + T, window=window, ring=ring)
-    p.dev.set_decode_path(*path)
+    p.dev.set_decode_path(path[0], path[1])
+    p.dev.set_row_slices(path[2])
     for b, L in enumerate(lens):
         k = _randn(1, L, Hkv, D, seed=100 + b)
         v = _randn(1, L, Hkv, D, seed=200 + b)
@@ -151,7 +155,7 @@ def test_decode_matches_oracle(case, path):
         return
     got, ref = p.decode(q, sinks=s)
     err = assert_close(got, ref)
-    if path != (2, 16):
+    if path[:2] != (2, 16):
         assert err <= 2e-5, f"fp32-level path error {err:.2e}"
     assert p.dev.device_error() == 0
 
@@ -261,14 +265,15 @@ def test_truncate_then_reappend_equals_clean_build():
     assert e.value.status == B.KVQ_ERANGE
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3], ids=["generic", "stream", "stream_rs2"])
 def test_ring_growth_matches_flat_oracle_and_keeps_invariants(path):
     """A small ring (window 64 + 31 rows) grown to 600 rows, T=1 steps: the
     live rows equal the oracle's logical rows, at most 31 masked rows precede
     the window, and outputs match the windowed oracle at every step."""
     Hq, Hkv, D, W, N = 16, 4, 64, 64, 600
     p = Pair(1, Hkv, D, Hq, max_t=1, window=W, ring=True)
-    p.dev.set_decode_path(path)
+    p.dev.set_decode_path(min(path, 2))
+    p.dev.set_row_slices(2 if path == 3 else 0)
     assert p.dev.rows == W + 31
     k = _randn(1, N, Hkv, D, seed=91)
     v = _randn(1, N, Hkv, D, seed=92)
@@ -294,7 +299,7 @@ def test_ring_growth_matches_flat_oracle_and_keeps_invariants(path):
     assert_close(got, ref)
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3], ids=["generic", "stream", "stream_rs2"])
 def test_ring_multi_row_chunks_match_windowed_oracle(path):
     """Prefill-style chunks on the ring: T-row appends (T drawn from 1..16, the
     ring sized window + 30 + max_t) each followed by the causal T-row decode;
@@ -302,7 +307,8 @@ def test_ring_multi_row_chunks_match_windowed_oracle(path):
     the windowed oracle, across many rebases."""
     Hq, Hkv, D, W, MT, N = 16, 4, 64, 256, 16, 1500
     p = Pair(1, Hkv, D, Hq, max_t=MT, window=W, ring=True)
-    p.dev.set_decode_path(path)
+    p.dev.set_decode_path(min(path, 2))
+    p.dev.set_row_slices(2 if path == 3 else 0)
     assert p.dev.rows == W + 30 + MT
     k = _randn(1, N, Hkv, D, seed=111)
     v = _randn(1, N, Hkv, D, seed=112)
@@ -327,7 +333,7 @@ def test_ring_multi_row_chunks_match_windowed_oracle(path):
     assert p.dev.device_error() == 0
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3], ids=["generic", "stream", "stream_rs2"])
 def test_ring_prime_chunks_match_windowed_oracle(path):
     """Prefill-sized chunks on the ring ("Module cache": the ring carries one
     whole maximum-size prime chunk beside the window): max_t = 512, the ring
@@ -338,7 +344,8 @@ def test_ring_prime_chunks_match_windowed_oracle(path):
     chunks = [512, 512, 100, 1, 512, 300, 7, 512, 33, 512, 1, 2, 512]
     N = sum(chunks)
     p = Pair(1, Hkv, D, Hq, max_t=MT, window=W, ring=True)
-    p.dev.set_decode_path(path)
+    p.dev.set_decode_path(min(path, 2))
+    p.dev.set_row_slices(2 if path == 3 else 0)
     assert p.dev.rows == W + 30 + MT
     k = _randn(1, N, Hkv, D, seed=121)
     v = _randn(1, N, Hkv, D, seed=122)
@@ -391,7 +398,8 @@ def test_ring_rebase_two_leg_route_matches_oracle(shape):
     assert p.dev.device_error() == 0
 
 
-@pytest.mark.parametrize("path", [(0, 0), (1, 0), (2, 16)], ids=["auto", "generic", "stream"])
+@pytest.mark.parametrize("path", [(0, 0, 0), (1, 0, 0), (2, 16, 0), (2, 16, 2)],
+                         ids=["auto", "generic", "stream", "stream_rs2"])
 @pytest.mark.parametrize("shape", [
     # B, Hq, Hkv, D, lens, T, window, sinks
     (2, 32, 8, 128, [700, 1500], 1, 0, True),
@@ -403,7 +411,8 @@ def test_decode_softcap_matches_oracle(shape, path):
     cap, and 0 turns it off again (bit-identical to the uncapped decode)."""
     Bn, Hq, Hkv, D, lens, T, window, sinks = shape
     p = Pair(Bn, Hkv, D, Hq, max_t=max(T, 64), max_rows=max(lens) + T, window=window)
-    p.dev.set_decode_path(*path)
+    p.dev.set_decode_path(path[0], path[1])
+    p.dev.set_row_slices(path[2])
     for b, L in enumerate(lens):
         k = _randn(1, L, Hkv, D, seed=300 + b)
         v = _randn(1, L, Hkv, D, seed=400 + b)
