@@ -449,6 +449,10 @@ def test_flat_capacity_errors_enqueue_nothing():
     with pytest.raises(B.KvqError) as e:
         c.decode(torch.zeros(1, 5, 4, 64, device="cuda"))
     assert e.value.status == B.KVQ_EINVAL      # T above max_t
+    for bad in (-1, 3):
+        with pytest.raises(B.KvqError) as e:
+            c.set_row_slices(bad)
+        assert e.value.status == B.KVQ_EINVAL
     assert c.device_error() == 0
 
 
