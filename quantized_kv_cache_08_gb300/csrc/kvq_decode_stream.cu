@@ -423,6 +423,85 @@ __device__ __forceinline__ void head_scores(const uint4* kc, const uint8_t* qw, 
     });
 }
 
+// The same scores read in 8-byte chunks from the head's first byte (8-byte
+// aligned for head_dim 128: 136 g), so every head runs one code path; with
+// one row slice per tile both 16-byte phases of the 16-byte reads would be
+// live at once and double the hot code.
+template <int QPL, int NQB, int O>
+__device__ __forceinline__ void block_scores8(const uint2* __restrict__ kc, const uint8_t* __restrict__ qw,
+                                              const uint8_t* __restrict__ lw, float (&s)[QPL]) {
+    constexpr int C0 = O >> 3;
+    constexpr int NC = ((O + 35) >> 3) - C0 + 1;
+    uint2 c[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) c[k] = kc[C0 + k];
+    auto word = [&](int byte) -> uint32_t {
+        const int rel = byte - C0 * 8;
+        const uint2& ch = c[rel >> 3];
+        return ((rel >> 2) & 1) ? ch.y : ch.x;
+    };
+    int acc[QPL];
+#pragma unroll
+    for (int j = 0; j < QPL; ++j) acc[j] = 0;
+#pragma unroll
+    for (int mp = 0; mp < 8; ++mp) {
+        uint32_t w[QPL][2];
+        if constexpr (QPL == 4) {
+            const uint4 a = *reinterpret_cast<const uint4*>(qw + mp * 32);
+            const uint4 b = *reinterpret_cast<const uint4*>(qw + mp * 32 + 16);
+            w[0][0] = a.x; w[0][1] = a.y; w[1][0] = a.z; w[1][1] = a.w;
+            w[2][0] = b.x; w[2][1] = b.y; w[3][0] = b.z; w[3][1] = b.w;
+        } else if constexpr (QPL == 2) {
+            const uint4 a = *reinterpret_cast<const uint4*>(qw + mp * 32);
+            w[0][0] = a.x; w[0][1] = a.y; w[1][0] = a.z; w[1][1] = a.w;
+        } else {
+            const uint2 a = *reinterpret_cast<const uint2*>(qw + mp * 32);
+            w[0][0] = a.x; w[0][1] = a.y;
+        }
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int pos = O + 2 + 2 * (2 * mp + h2);
+            const uint32_t cw = word(pos);
+#pragma unroll
+            for (int j = 0; j < QPL; ++j)
+                acc[j] = ((pos >> 1) & 1) ? dp2a_hi(w[j][h2], cw, acc[j]) : dp2a_lo(w[j][h2], cw, acc[j]);
+        }
+    }
+    float tot[QPL];
+    if constexpr (NQB == 24) {
+        constexpr bool mis = (O & 3) == 0;
+        constexpr int NW = mis ? 9 : 8;
+        constexpr int B0 = mis ? O : O + 2;
+        int accl[QPL];
+#pragma unroll
+        for (int j = 0; j < QPL; ++j) accl[j] = 0;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            const uint32_t cw = word(B0 + 4 * k);
+#pragma unroll
+            for (int j = 0; j < QPL; ++j)
+                accl[j] = dp4a_su(cw, *reinterpret_cast<const uint32_t*>(lw + k * 16 + 4 * j), accl[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < QPL; ++j) tot[j] = fmaf(256.f, (float)acc[j], (float)accl[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < QPL; ++j) tot[j] = (float)acc[j];
+    }
+    const uint32_t dw = word(O);
+    const float d = h2f(((O >> 1) & 1) ? (dw >> 16) : (dw & 0xffffu));
+#pragma unroll
+    for (int j = 0; j < QPL; ++j) s[j] = fmaf(d, tot[j], s[j]);
+}
+
+template <int NBH, int QPL, int NQB>
+__device__ __forceinline__ void head_scores8(const uint2* kc, const uint8_t* qw, const uint8_t* lw, float (&s)[QPL]) {
+    static_for<0, NBH>([&](auto I) {
+        constexpr int i = decltype(I)::value;
+        block_scores8<QPL, NQB, 34 * i>(kc, qw + i * 256, lw + i * 144, s);
+    });
+}
+
 // PH = (34 * NBH * g) mod 16, the offset of the head's first block in its
 // 16-byte chunk: 0 for NBH = 8, {0, 8} for NBH = 4, {0, 4, 8, 12} for NBH = 2
 template <int NBH, int QPL, int NQB>
@@ -820,7 +899,11 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) KVQ_STREAM_KERNEL(
 #if KVQ_STREAM_F8
             head_scores_f8<NBH, QPL>(kc, reinterpret_cast<const float*>(smem + w_off) + kp * QPL * 4, sc);
 #else
-            head_scores_ph<NBH, QPL, NQB>(ph, kc, smem + w_off + kp * QPL * 8, smem + lw_off + kp * QPL * 4, sc);
+            if constexpr (NBH == 4 && KP == 1)
+                head_scores8<NBH, QPL, NQB>(reinterpret_cast<const uint2*>(smem + k_lane_off + ph + (uint32_t)st * L.kstage),
+                                            smem + w_off + kp * QPL * 8, smem + lw_off + kp * QPL * 4, sc);
+            else
+                head_scores_ph<NBH, QPL, NQB>(ph, kc, smem + w_off + kp * QPL * 8, smem + lw_off + kp * QPL * 4, sc);
 #endif
         }
         // ------------------------------------------------ online softmax
