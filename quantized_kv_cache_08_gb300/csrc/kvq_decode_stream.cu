@@ -424,9 +424,9 @@ __device__ __forceinline__ void head_scores(const uint4* kc, const uint8_t* qw, 
 }
 
 // The same scores read in 8-byte chunks from the head's first byte (8-byte
-// aligned for head_dim 128: 136 g), so every head runs one code path; with
-// one row slice per tile both 16-byte phases of the 16-byte reads would be
-// live at once and double the hot code.
+// aligned for head_dim 128: 136 g), so every head runs one code path: with
+// 16-byte reads the heads of odd g start 8 bytes into a chunk and need their
+// own unrolled path, and both paths are live at once, doubling the hot code.
 template <int QPL, int NQB, int O>
 __device__ __forceinline__ void block_scores8(const uint2* __restrict__ kc, const uint8_t* __restrict__ qw,
                                               const uint8_t* __restrict__ lw, float (&s)[QPL]) {
@@ -899,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) KVQ_STREAM_KERNEL(
 #if KVQ_STREAM_F8
             head_scores_f8<NBH, QPL>(kc, reinterpret_cast<const float*>(smem + w_off) + kp * QPL * 4, sc);
 #else
-            if constexpr (NBH == 4 && KP == 1)
+            if constexpr (NBH == 4)
                 head_scores8<NBH, QPL, NQB>(reinterpret_cast<const uint2*>(smem + k_lane_off + ph + (uint32_t)st * L.kstage),
                                             smem + w_off + kp * QPL * 8, smem + lw_off + kp * QPL * 4, sc);
             else
