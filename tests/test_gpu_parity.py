@@ -129,12 +129,12 @@ CASES = [
 
 # (kernel path, query bits): 1 = generic split kernel, 2 = stream-K kernel
 # (kernel path, query bits, row slices): the generic kernel, the stream-K
-# kernel with 24- and 16-bit queries, and the stream-K kernel with two row
-# slices forced (small shapes otherwise take one: few tiles per CTA)
-PATHS = [(1, 0, 0), (2, 24, 0), (2, 16, 0), (2, 16, 2)]
+# kernel with 24- and 16-bit queries, each also with two row slices forced
+# (small shapes otherwise take one: few tiles per CTA)
+PATHS = [(1, 0, 0), (2, 24, 0), (2, 16, 0), (2, 16, 2), (2, 24, 2)]
 
 
-@pytest.mark.parametrize("path", PATHS, ids=["generic", "ws24", "ws16", "ws16rs2"])
+@pytest.mark.parametrize("path", PATHS, ids=["generic", "ws24", "ws16", "ws16rs2", "ws24rs2"])
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
 def test_decode_matches_oracle(case, path):
     Bn, Hq, Hkv, D, lens, T, window, ring, sinks, qdt = case
